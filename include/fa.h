@@ -1,0 +1,175 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) tiled exact attention library (libfa.so).
+ *
+ * What is computed (the plain definition, "hs-black: FlashAttention 1/2/3",
+ * section "Shapes"; LSE from "One row of runnable logic"):
+ *
+ *   for every batch b, query head h, query row i:
+ *     kv_head  = h / (hq / hkv)                      (GQA mapping, "flash attention V2
+ *                                                     code walkthrough", block_table / h_h_k_ratio)
+ *     visible  = { j < skv : !causal || j <= i + q_pos_offset }
+ *     s_j      = scale * <Q[b,i,h,:], K[b,j,kv_head,:]>
+ *     O[b,i,h] = sum_j softmax(s)_j V[b,j,kv_head,:]   over visible j
+ *     LSE[b,h,i] = log sum_j exp(s_j)                  over visible j
+ *   A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * The causal rule is bottom-right aligned by default (q_pos_offset = skv - sq,
+ * the mask pictures of "flash attention V2 code walkthrough", Is_causal); any
+ * other offset gives the absolute query position used by a KV-cache decode
+ * ("hs-black", section "Implementation: causal and tail blocks").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  Split-KV needs a caller-owned
+ *     device workspace (see fa_splitkv_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call is asynchronous on that stream; results are ready
+ *     when the stream is synchronised.
+ *   - Validation happens on the host before any launch; an invalid argument
+ *     returns an error code and launches nothing.  No exception crosses the ABI.
+ *   - Device-side waits are bounded (about two seconds each); a wait that runs
+ *     out is recorded in a per-device status word that fa_sync_status reports.
+ *   - Layouts: Q, O are [b, sq, hq, d] and K, V are [b, skv, hkv, d] with the
+ *     head dimension contiguous and the other three strides given in elements
+ *     (order: batch, row, head).  LSE is fp32 [b, hq, sq], contiguous.
+ *   - Supported: d in {64, 128, 256}; bf16 or fp16 storage; fp32 accumulation.
+ *     Base pointers 16-byte aligned; strides multiples of 8 elements.
+ */
+#ifndef TILED_EXACT_ATTENTION_FA_H
+#define TILED_EXACT_ATTENTION_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, stride or alignment */
+  FA_ERR_UNSUPPORTED = 2, /* a head dimension or shape outside the compiled set */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
+  FA_ERR_TIMEOUT = 4      /* a device-side wait gave up (reported by fa_sync_status) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/* q_pos_offset value meaning "bottom-right aligned": skv - sq. */
+#define FA_OFFSET_BOTTOM_RIGHT INT64_MIN
+
+typedef struct {
+  fa_dtype dtype;     /* storage type of Q, K, V and O */
+  int32_t b;          /* batch */
+  int32_t sq;         /* query rows per sequence (>= 0) */
+  int32_t skv;        /* key rows per sequence (>= 0) */
+  int32_t hq;         /* query heads (>= 1) */
+  int32_t hkv;        /* key/value heads, hq % hkv == 0 */
+  int32_t d;          /* head dimension: 64, 128 or 256 */
+  const void* q;      /* device, [b, sq, hq, d] */
+  const void* k;      /* device, [b, skv, hkv, d] */
+  const void* v;      /* device, [b, skv, hkv, d] */
+  void* o;            /* device, [b, sq, hq, d], written */
+  float* lse;         /* device, fp32 [b, hq, sq], written */
+  int64_t q_strides[3]; /* (batch, row, head) strides of q, in elements */
+  int64_t k_strides[3];
+  int64_t v_strides[3];
+  int64_t o_strides[3];
+  int32_t causal;       /* 0 or 1 */
+  int64_t q_pos_offset; /* causal: row i sees key j iff j <= i + q_pos_offset;
+                           FA_OFFSET_BOTTOM_RIGHT = skv - sq.  Ignored when causal == 0. */
+  float scale;          /* multiplies q.k before the mask and the max; finite, > 0 (e.g. 1/sqrt(d)) */
+} fa_fwd_args;
+
+/*
+ * Prefill / general forward pass: O and LSE for every row.
+ * Tiled exactly as "ai-reference-codex: forward CUDA kernel", sections 2-6: a
+ * CTA owns Q row blocks, K/V blocks stream past, blocks beyond the causal
+ * diagonal are skipped, the elementwise mask runs only on diagonal and tail
+ * blocks, and the epilogue divides by l and writes LSE = m + log l.
+ * Returns FA_OK once the work is enqueued on `stream`.
+ */
+fa_status fa_fwd(const fa_fwd_args* args, void* stream);
+
+/*
+ * Split count for split-KV ("ai-reference-codex: forward CUDA kernel", 7.2):
+ * with w(s) = units * s / slots and efficiency(s) = w / ceil(w), return the
+ * smallest s in [1, min(max_splits, num_kv_blocks)] whose efficiency is at least
+ * 85% of the best one.  units = independent CTAs before splitting, slots =
+ * concurrently resident CTAs (SMs x CTAs per SM).  Pure host function.
+ * Returns 1 for non-positive units or slots.
+ */
+int32_t fa_num_splits_heuristic(int64_t units, int64_t slots, int64_t num_kv_blocks, int32_t max_splits);
+
+/*
+ * The split count fa_fwd_splitkv would use for `args` with num_splits == 0 on
+ * the current device (the heuristic above applied to this launch).  Returns
+ * 0 and writes nothing if the arguments are invalid.
+ */
+int32_t fa_splitkv_default_splits(const fa_fwd_args* args);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for `num_splits` splits (0 = the
+ * default count): fp32 partial outputs [num_splits, b, hq, sq, d] followed
+ * (256-byte aligned) by fp32 partial LSEs [num_splits, b, hq, sq].
+ * Returns 0 for invalid arguments.
+ */
+size_t fa_splitkv_workspace_size(const fa_fwd_args* args, int32_t num_splits);
+
+/*
+ * Split-KV forward ("ai-reference-codex: forward CUDA kernel", section 7; the
+ * early-exit rule of "flash attention V2 code walkthrough",
+ * compute_attn_1rowblock_splitkv): the key blocks are cut into num_splits
+ * contiguous ranges of ceil(nblk / num_splits) blocks; split s writes its
+ * normalised partial O_s and LSE_s into the workspace (0 and -inf for a split
+ * with no visible key), then fa_splitkv_combine merges them into args->o and
+ * args->lse.  For sq == 1 the query heads sharing a KV head are folded into
+ * one CTA (section 7.4).  num_splits == 0 picks the count with the heuristic;
+ * the count used is written to *splits_used (may be NULL).  The workspace is a
+ * caller-owned device buffer of at least fa_splitkv_workspace_size bytes,
+ * 256-byte aligned.  Same result as fa_fwd up to rounding.
+ */
+fa_status fa_fwd_splitkv(const fa_fwd_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                         int32_t* splits_used, void* stream);
+
+/*
+ * LSE-weighted merge of split partials ("ai-reference-codex: forward CUDA
+ * kernel", 7.3): per row, LSE = logsumexp_s LSE_s and O = sum_s
+ * e^(LSE_s - LSE) O_s; if every LSE_s is -inf the row gets O = 0, LSE = -inf.
+ *   o_part:   device fp32 [num_splits, b, hq, sq, d] (normalised partials)
+ *   lse_part: device fp32 [num_splits, b, hq, sq]
+ *   o:        device [b, sq, hq, d] of `dtype`, strides (batch, row, head) in elements
+ *   lse:      device fp32 [b, hq, sq], or NULL to skip it
+ * 1 <= num_splits; d in {64, 128, 256}.
+ */
+fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t b,
+                             int32_t hq, int32_t sq, int32_t d, fa_dtype dtype, void* o,
+                             const int64_t o_strides[3], float* lse, void* stream);
+
+/*
+ * Synchronise `stream` and report device-side failures on the current device:
+ * FA_ERR_TIMEOUT if any kernel of this library recorded a wait that ran out
+ * since the last call (the record is then cleared), FA_ERR_CUDA if the
+ * synchronisation itself failed, FA_OK otherwise.
+ */
+fa_status fa_sync_status(void* stream);
+
+/*
+ * Self-test of the bounded-wait path: launches one tiny kernel that waits on
+ * a barrier nothing completes.  The wait gives up after its limit (about two
+ * seconds), records a timeout and returns, so that a following
+ * fa_sync_status returns FA_ERR_TIMEOUT while the context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(void* stream);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status status);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_EXACT_ATTENTION_FA_H */

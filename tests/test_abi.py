@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/fa.h declares, validates arguments before touching the
+device, and its split heuristic agrees with the oracle's."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from tiled_exact_attention_gb300 import build as b
+
+    b.build()
+    from tiled_exact_attention_gb300 import _lib
+
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_function(lib):
+    from tiled_exact_attention_gb300 import _lib
+
+    declared = _declared_functions()
+    assert len(declared) >= 9
+    assert sorted(_lib.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() == 1
+    for code in range(5):
+        assert lib.fa_status_string(code)
+    assert lib.fa_status_string(99) == b"unknown status"
+
+
+def test_heuristic_matches_oracle(lib, oracle_mod):
+    for units in (1, 3, 8, 48, 64, 100, 152, 300, 1024):
+        for slots in (108, 148, 152, 304):
+            for nblk in (1, 2, 7, 64, 512):
+                assert lib.fa_num_splits_heuristic(units, slots, nblk, 128) == \
+                    oracle_mod.num_splits(units, slots, nblk, 128), (units, slots, nblk)
+    assert lib.fa_num_splits_heuristic(48, 108, 1000, 128) == 2
+    assert lib.fa_num_splits_heuristic(0, 108, 10, 128) == 1
+
+
+def _args(**kw):
+    from tiled_exact_attention_gb300._lib import FwdArgs
+
+    a = FwdArgs()
+    a.dtype, a.b, a.sq, a.skv, a.hq, a.hkv, a.d = 0, 1, 128, 128, 2, 2, 128
+    for f in ("q_strides", "k_strides", "v_strides", "o_strides"):
+        setattr(a, f, (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128))
+    a.q = a.k = a.v = a.o = 4096
+    a.lse = 4096
+    a.causal = 0
+    a.scale = 0.125
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("dtype", 7, 1), ("b", 0, 1), ("hq", 3, 1), ("causal", 2, 1), ("scale", 0.0, 1),
+    ("scale", float("nan"), 1), ("d", 96, 2), ("d", 32, 2), ("q", 0, 1), ("lse", 0, 1), ("q", 4100, 1),
+])
+def test_validation_rejects_before_any_launch(lib, field, value, expect):
+    a = _args(**{field: value})
+    assert lib.fa_fwd(ctypes.byref(a), None) == expect
+    assert lib.fa_fwd_splitkv(ctypes.byref(a), 1, None, 0, None, None) == expect
+
+
+def test_validation_strides_and_null(lib):
+    a = _args()
+    a.q_strides = (ctypes.c_int64 * 3)(100, 20, 4)  # not multiples of 8 elements
+    assert lib.fa_fwd(ctypes.byref(a), None) == 1
+    assert lib.fa_fwd(None, None) == 1
+    a = _args(sq=0)
+    assert lib.fa_fwd(ctypes.byref(a), None) == 0  # nothing to do
+    assert lib.fa_splitkv_workspace_size(None, 1) == 0
+    a = _args()
+    ws = lib.fa_splitkv_workspace_size(ctypes.byref(a), 3)
+    rows = 3 * 1 * 2 * 128
+    assert ws >= rows * 128 * 4 + rows * 4
+    assert lib.fa_fwd_splitkv(ctypes.byref(a), -1, None, 0, None, None) == 1
+
+
+def test_combine_validation(lib):
+    st = (ctypes.c_int64 * 3)(1, 1, 1)
+    assert lib.fa_splitkv_combine(None, None, 0, 1, 1, 1, 64, 0, None, st, None, None) == 1
+    assert lib.fa_splitkv_combine(None, None, 1, 1, 1, 1, 80, 0, None, st, None, None) == 2
+    assert lib.fa_splitkv_combine(None, None, 1, 1, 1, 0, 64, 0, None, st, None, None) == 0

@@ -1,0 +1,17 @@
+"""GB300-native tiled exact attention (FlashAttention forward + split-KV decode).
+
+The computation runs in libfa.so (hand-written sm_103a CUDA); this package only
+marshals torch tensors into the C ABI of include/fa.h.
+"""
+from .api import (  # noqa: F401
+    fa_fwd,
+    fa_fwd_splitkv,
+    fa_num_splits_heuristic,
+    fa_selftest_wait_timeout,
+    fa_splitkv_combine,
+    fa_splitkv_default_splits,
+    fa_splitkv_workspace_size,
+    fa_sync_status,
+    fa_version,
+)
+from ._lib import FaError  # noqa: F401

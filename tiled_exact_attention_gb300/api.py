@@ -1,0 +1,149 @@
+"""Python entry points with the same names as the C ABI (argument marshalling only).
+
+Tensors are torch CUDA tensors: Q, O ``[b, sq, hq, d]``, K, V ``[b, skv, hkv, d]``
+(head dimension contiguous), LSE fp32 ``[b, hq, sq]``.  PyTorch provides the
+device memory and the current stream; every step of the computation runs in
+libfa.so.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, check
+
+_DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _strides(t: torch.Tensor):
+    s = t.stride()
+    return (ctypes.c_int64 * 3)(s[0], s[1], s[2])
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [b, s, h, d]")
+        if t.dtype not in _DT:
+            raise ValueError(f"{name} must be bf16 or fp16")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name} must have a contiguous head dimension")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("inconsistent q/k/v shapes")
+
+
+def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offset: int | None) -> FwdArgs:
+    _check_qkv(q, k, v)
+    b, sq, hq, d = q.shape
+    skv, hkv = k.shape[1], k.shape[2]
+    a = FwdArgs()
+    a.dtype = _DT[q.dtype]
+    a.b, a.sq, a.skv, a.hq, a.hkv, a.d = b, sq, skv, hq, hkv, d
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.o, a.lse = o.data_ptr(), lse.data_ptr()
+    a.q_strides, a.k_strides, a.v_strides, a.o_strides = _strides(q), _strides(k), _strides(v), _strides(o)
+    a.causal = 1 if causal else 0
+    a.q_pos_offset = FA_OFFSET_BOTTOM_RIGHT if q_pos_offset is None else int(q_pos_offset)
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    return a
+
+
+def _outputs(q, out, lse):
+    b, sq, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, hq, sq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_cuda or out.stride(3) != 1:
+        raise ValueError("out must match q")
+    if lse.shape != (b, hq, sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [b, hq, sq]")
+    return out, lse
+
+
+def fa_fwd(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
+           out=None, lse=None, stream=None):
+    """Forward pass; returns (O, LSE)."""
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    check(_lib.load().fa_fwd(ctypes.byref(a), _stream_handle(stream)), "fa_fwd")
+    return out, lse
+
+
+def fa_num_splits_heuristic(units: int, slots: int, num_kv_blocks: int, max_splits: int = 128) -> int:
+    return int(_lib.load().fa_num_splits_heuristic(units, slots, num_kv_blocks, max_splits))
+
+
+def fa_splitkv_default_splits(q, k, v, *, causal=False, scale=None, q_pos_offset=None) -> int:
+    out, lse = _outputs(q, None, None)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    return int(_lib.load().fa_splitkv_default_splits(ctypes.byref(a)))
+
+
+def fa_splitkv_workspace_size(q, k, v, num_splits: int = 0, *, causal=False, scale=None,
+                              q_pos_offset=None) -> int:
+    out, lse = _outputs(q, None, None)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    return int(_lib.load().fa_splitkv_workspace_size(ctypes.byref(a), num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
+                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None, return_splits=False):
+    """Split-KV forward + combine; returns (O, LSE) (and the split count if asked)."""
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    lib = _lib.load()
+    need = int(lib.fa_splitkv_workspace_size(ctypes.byref(a), int(num_splits)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    used = ctypes.c_int32(0)
+    check(lib.fa_fwd_splitkv(ctypes.byref(a), int(num_splits), ctypes.c_void_p(workspace.data_ptr()),
+                             workspace.numel() * workspace.element_size(), ctypes.byref(used),
+                             _stream_handle(stream)), "fa_fwd_splitkv")
+    if return_splits:
+        return out, lse, int(used.value)
+    return out, lse
+
+
+def fa_splitkv_combine(o_part, lse_part, out, lse=None, stream=None):
+    """Merge fp32 partials o_part [ns, b, hq, sq, d], lse_part [ns, b, hq, sq] into out [b, sq, hq, d]."""
+    ns, b, hq, sq, d = o_part.shape
+    if not (o_part.is_cuda and lse_part.is_cuda and out.is_cuda):
+        raise ValueError("tensors must be on the GPU")
+    if o_part.dtype != torch.float32 or lse_part.dtype != torch.float32 or not o_part.is_contiguous() \
+            or not lse_part.is_contiguous() or lse_part.shape != (ns, b, hq, sq):
+        raise ValueError("partials must be contiguous fp32")
+    if out.dtype not in _DT or out.shape != (b, sq, hq, d) or out.stride(3) != 1:
+        raise ValueError("out must be [b, sq, hq, d] bf16/fp16")
+    st = _strides(out)
+    lp = ctypes.c_void_p(lse.data_ptr()) if lse is not None else ctypes.c_void_p(0)
+    check(_lib.load().fa_splitkv_combine(ctypes.c_void_p(o_part.data_ptr()), ctypes.c_void_p(lse_part.data_ptr()),
+                                         ns, b, hq, sq, d, _DT[out.dtype], ctypes.c_void_p(out.data_ptr()), st, lp,
+                                         _stream_handle(stream)), "fa_splitkv_combine")
+    return out, lse
+
+
+def fa_sync_status(stream=None) -> int:
+    """Synchronise the stream; return the status code (0 = ok, 4 = a device wait timed out)."""
+    return int(_lib.load().fa_sync_status(_stream_handle(stream)))
+
+
+def fa_selftest_wait_timeout(stream=None) -> None:
+    check(_lib.load().fa_selftest_wait_timeout(_stream_handle(stream)), "fa_selftest_wait_timeout")
+
+
+def fa_version() -> int:
+    return int(_lib.load().fa_version())

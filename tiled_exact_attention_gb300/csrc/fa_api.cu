@@ -1,0 +1,407 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, the split-count heuristic, launches and status codes.
+// No allocation happens here: every buffer, including the split-KV workspace,
+// belongs to the caller.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// One status word per device: kernels record the first wait that ran out.
+__device__ int g_fa_status;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 128;
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int* status = nullptr;
+  int sms = 0;
+};
+
+bool device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& di = cache[dev];
+  if (di.status == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    di.status = static_cast<int*>(p);
+    di.sms = sms;
+  }
+  *out = di;
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool strides_ok(const int64_t s[3]) {
+  for (int i = 0; i < 3; ++i) {
+    if (s[i] <= 0 || (s[i] % 8) != 0) return false;
+    if (s[i] * 2 >= (static_cast<int64_t>(1) << 40)) return false;
+  }
+  return true;
+}
+
+fa_status validate(const fa_fwd_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->sq < 0 || a->skv < 0 || a->hq < 1 || a->hkv < 1) return FA_ERR_INVALID_ARG;
+  if (a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
+  if (a->sq > (1 << 30) || a->skv > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (a->sq == 0) return FA_OK;
+  if (a->q == nullptr || a->o == nullptr || a->lse == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4)) return FA_ERR_INVALID_ARG;
+  if (!strides_ok(a->q_strides) || !strides_ok(a->o_strides)) return FA_ERR_INVALID_ARG;
+  if (a->skv > 0) {
+    if (a->k == nullptr || a->v == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(a->k, 16) || !aligned(a->v, 16)) return FA_ERR_INVALID_ARG;
+    if (!strides_ok(a->k_strides) || !strides_ok(a->v_strides)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+// 4-D tiled map over [b][s][h][d] storage: dims (d, h, s, b), box (inner, 1, rows, 1).
+bool encode_map(CUtensorMap* m, const void* ptr, fa_dtype dt, int d, int h, int s, int b, const int64_t st[3],
+                int box_inner, int box_rows, bool swizzle128) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h),
+                        static_cast<cuuint64_t>(s > 0 ? s : 1), static_cast<cuuint64_t>(b)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                           static_cast<cuuint64_t>(st[0]) * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = dt == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Causal offset as the kernels use it: j <= i + off.  Returns false when the
+// causal constraint hides nothing (then the problem is treated as non-causal).
+struct CausalPlan {
+  int causal;
+  int off;
+};
+
+CausalPlan plan_causal(const fa_fwd_args* a) {
+  CausalPlan c{0, 0};
+  if (!a->causal) return c;
+  int64_t off = a->q_pos_offset == FA_OFFSET_BOTTOM_RIGHT ? static_cast<int64_t>(a->skv) - a->sq : a->q_pos_offset;
+  if (off >= static_cast<int64_t>(a->skv) - 1) return c;  // row 0 already sees every key
+  if (off < -static_cast<int64_t>(a->sq) - 1) off = -static_cast<int64_t>(a->sq) - 1;  // every row sees nothing
+  c.causal = 1;
+  c.off = static_cast<int>(off);
+  return c;
+}
+
+bool use_decode_kernel(const fa_fwd_args* a) { return a->sq == 1 && decode_supported(a->d, a->hq / a->hkv); }
+
+// Keys a decode row can see (sq == 1): j < kv_limit.
+int decode_kv_limit(const fa_fwd_args* a) {
+  const CausalPlan c = plan_causal(a);
+  if (!c.causal) return a->skv;
+  const int64_t lim = static_cast<int64_t>(c.off) + 1;
+  return static_cast<int>(lim < 0 ? 0 : (lim > a->skv ? a->skv : lim));
+}
+
+struct SplitShape {
+  int64_t units;
+  int64_t slots;
+  int64_t nblk;
+};
+
+bool split_shape(const fa_fwd_args* a, const DeviceInfo& di, SplitShape* s) {
+  if (use_decode_kernel(a)) {
+    const int g = a->hq / a->hkv;
+    s->units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
+    s->slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
+    s->nblk = ceil_div64(decode_kv_limit(a), decode_block_n(a->d));
+  } else {
+    const int nq = prefill_q_tiles(a->d);
+    const int64_t n_mcta = ceil_div64(ceil_div64(a->sq, 128), nq);
+    s->units = static_cast<int64_t>(a->b) * a->hq * n_mcta;
+    s->slots = di.sms;
+    s->nblk = ceil_div64(a->skv, prefill_block_n(a->d));
+  }
+  return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t workspace_bytes_for(const fa_fwd_args* a, int ns) {
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq * a->sq;
+  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+int resolve_splits(const fa_fwd_args* a, int32_t requested, const DeviceInfo& di) {
+  SplitShape s{};
+  split_shape(a, di, &s);
+  int ns = requested > 0 ? requested
+                         : fa_num_splits_heuristic(s.units, s.slots, s.nblk, kMaxSplits);
+  const int64_t cap = s.nblk > 0 ? s.nblk : 1;
+  if (ns > cap) ns = static_cast<int>(cap);
+  if (ns > kMaxSplits * 8) ns = kMaxSplits * 8;
+  return ns < 1 ? 1 : ns;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int32_t fa_version(void) { return 1; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape or head dimension";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t fa_num_splits_heuristic(int64_t units, int64_t slots, int64_t num_kv_blocks, int32_t max_splits) {
+  if (units <= 0 || slots <= 0) return 1;
+  int64_t smax = max_splits < num_kv_blocks ? max_splits : num_kv_blocks;
+  if (smax < 1) smax = 1;
+  auto eff = [&](int64_t s) {
+    const double w = static_cast<double>(units * s) / static_cast<double>(slots);
+    return w / std::ceil(w);
+  };
+  double best = 0.0;
+  for (int64_t s = 1; s <= smax; ++s) best = eff(s) > best ? eff(s) : best;
+  for (int64_t s = 1; s <= smax; ++s)
+    if (eff(s) >= 0.85 * best) return static_cast<int32_t>(s);
+  return 1;
+}
+
+fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
+  const fa_status v = validate(a);
+  if (v != FA_OK || a->sq == 0) return v;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int bn = prefill_block_n(a->d);
+  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->sq, a->b, a->q_strides, 64, 128, true) ||
+      !encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->sq, a->b, a->o_strides, 64, 128, true))
+    return FA_ERR_INVALID_ARG;
+  if (a->skv > 0 &&
+      (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
+       !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, bn, true)))
+    return FA_ERR_INVALID_ARG;
+  const CausalPlan c = plan_causal(a);
+  p.o = a->o;
+  p.lse = a->lse;
+  p.o_part = nullptr;
+  p.o_stride_b = a->o_strides[0];
+  p.o_stride_row = a->o_strides[1];
+  p.o_stride_h = a->o_strides[2];
+  p.b = a->b;
+  p.sq = a->sq;
+  p.skv = a->skv;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.causal = c.causal;
+  p.off = c.off;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
+  p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+  p.num_splits = 1;
+  p.blocks_per_split = static_cast<int>(ceil_div64(a->skv, bn));
+  p.status = di.status;
+  return from_cuda(launch_prefill(p, a->d, a->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t fa_splitkv_default_splits(const fa_fwd_args* a) {
+  if (validate(a) != FA_OK) return 0;
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  return resolve_splits(a, 0, di);
+}
+
+size_t fa_splitkv_workspace_size(const fa_fwd_args* a, int32_t num_splits) {
+  if (validate(a) != FA_OK || num_splits < 0) return 0;
+  int ns = num_splits;
+  if (ns == 0) {
+    DeviceInfo di;
+    if (!device_info(&di)) return 0;
+    ns = resolve_splits(a, 0, di);
+  }
+  return workspace_bytes_for(a, ns);
+}
+
+fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t b, int32_t hq,
+                             int32_t sq, int32_t d, fa_dtype dtype, void* o, const int64_t o_strides[3],
+                             float* lse, void* stream) {
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (num_splits < 1 || b < 1 || hq < 1 || sq < 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (sq == 0) return FA_OK;
+  if (o_part == nullptr || lse_part == nullptr || o == nullptr || o_strides == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 4) || !aligned(lse_part, 4) || !aligned(o, 2) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (o_strides[i] <= 0) return FA_ERR_INVALID_ARG;
+  CombineParams p;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.o = o;
+  p.o_stride_b = o_strides[0];
+  p.o_stride_row = o_strides[1];
+  p.o_stride_h = o_strides[2];
+  p.lse = lse;
+  p.num_splits = num_splits;
+  p.b = b;
+  p.hq = hq;
+  p.sq = sq;
+  p.d = d;
+  return from_cuda(launch_combine(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                         int32_t* splits_used, void* stream) {
+  const fa_status v = validate(a);
+  if (v != FA_OK) return v;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (a->sq == 0) {
+    if (splits_used) *splits_used = 0;
+    return FA_OK;
+  }
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  const int ns = resolve_splits(a, num_splits, di);
+  const size_t need = workspace_bytes_for(a, ns);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
+  float* o_part = static_cast<float*>(workspace);
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq * a->sq;
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * a->d * sizeof(float)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  cudaError_t e;
+  if (use_decode_kernel(a)) {
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int bn = decode_block_n(a->d);
+    if (a->skv > 0 &&
+        (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, a->d, bn, false) ||
+         !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, a->d, bn, false)))
+      return FA_ERR_INVALID_ARG;
+    p.q = a->q;
+    p.q_stride_b = a->q_strides[0];
+    p.q_stride_h = a->q_strides[2];
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.b = a->b;
+    p.skv = a->skv;
+    p.hq = a->hq;
+    p.hkv = a->hkv;
+    p.g = a->hq / a->hkv;
+    p.kv_limit = decode_kv_limit(a);
+    p.nblk = static_cast<int>(ceil_div64(p.kv_limit, bn));
+    p.num_splits = ns;
+    p.blocks_per_split = static_cast<int>(ceil_div64(p.nblk > 0 ? p.nblk : 1, ns));
+    p.scale_log2 = scale_log2;
+    p.status = di.status;
+    e = launch_decode(p, a->d, a->dtype, st);
+  } else {
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int bn = prefill_block_n(a->d);
+    if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->sq, a->b, a->q_strides, 64, 128, true))
+      return FA_ERR_INVALID_ARG;
+    if (a->skv > 0 &&
+        (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
+         !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, bn, true)))
+      return FA_ERR_INVALID_ARG;
+    const CausalPlan c = plan_causal(a);
+    p.o = nullptr;
+    p.lse = lse_part;
+    p.o_part = o_part;
+    p.b = a->b;
+    p.sq = a->sq;
+    p.skv = a->skv;
+    p.hq = a->hq;
+    p.hkv = a->hkv;
+    p.g = a->hq / a->hkv;
+    p.causal = c.causal;
+    p.off = c.off;
+    p.scale_log2 = scale_log2;
+    p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
+    p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+    p.num_splits = ns;
+    const int64_t nblk = ceil_div64(a->skv, bn);
+    p.blocks_per_split = static_cast<int>(ceil_div64(nblk > 0 ? nblk : 1, ns));
+    p.status = di.status;
+    e = launch_prefill(p, a->d, a->dtype, st);
+  }
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (splits_used) *splits_used = ns;
+  return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, a->sq, a->d, a->dtype, a->o, a->o_strides, a->lse,
+                            stream);
+}
+
+fa_status fa_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (code != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(void* stream) {
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  return from_cuda(launch_wait_selftest(di.status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

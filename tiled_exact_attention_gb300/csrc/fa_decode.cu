@@ -1,0 +1,439 @@
+// Split-KV decode (one query row per head) and the LSE-weighted combine.
+//
+// Decode reads the whole KV cache once and does a few flops per byte, so it is
+// bound by HBM bandwidth, not by the tensor cores: it runs on the CUDA cores.
+// Following "ai-reference-codex: forward CUDA kernel", section 7:
+//  * 7.4: the g = hq / hkv query heads that share one KV head are folded into
+//    one CTA, so each K/V byte is read once for the whole group;
+//  * 7.1-7.2: the KV range is cut into num_splits contiguous block ranges, one
+//    CTA each, so that the grid fills the GPU;
+//  * 7.3: each split writes its normalised partial output and its LSE (-inf for
+//    a split with no visible key) and the combine kernel merges them with
+//    weights e^(LSE_s - LSE).
+// K/V blocks stream through a shared-memory ring filled by TMA; four compute
+// warps each take 16 rows of every block and keep their own running (m, l, o)
+// per head, merged across warps at the end of the split.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kDecBN = 64;          // keys per stage
+constexpr int kDecWarps = 4;        // compute warps
+constexpr int kDecRowsPerWarp = kDecBN / kDecWarps;
+
+template <int D>
+struct DecCfg {
+  static constexpr int STAGES = (D == 256) ? 2 : 3;
+  static constexpr int KV_BYTES = kDecBN * D * 2;        // one K or V block
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int THREADS = 32 * (kDecWarps + 1);
+  static constexpr int PRODUCER_WARP = kDecWarps;
+};
+
+template <int D, int G>
+struct DecLane {
+  static_assert(G == 1 || G == 2 || G == 4, "heads per CTA");
+  static constexpr int DPL = 16;                  // head dims per lane
+  static constexpr int SEG = DPL / 8;             // 16-byte segments per lane
+  static constexpr int LPR = D / DPL;             // lanes per key row
+  static constexpr int RPP = 32 / LPR;            // key rows per pass
+  static constexpr int PASSES = kDecRowsPerWarp / RPP;
+  static_assert(LPR <= 32 && 32 % LPR == 0, "lane layout");
+  static_assert(PASSES >= 1, "rows per warp");
+};
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    } else {
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_elem(const void* base, int64_t idx) {
+  const uint16_t u = static_cast<const uint16_t*>(base)[idx];
+  if constexpr (BF16) {
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  } else {
+    return __half2float(__ushort_as_half(u));
+  }
+}
+
+enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
+
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecCfg<D>;
+  using L = DecLane<D, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  float* red = reinterpret_cast<float*>(empty + C::STAGES);  // [warps][G][D + 2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, bi = blockIdx.z;
+  const int groups = p.g / G;                    // CTAs per KV head
+  const int kvh = blockIdx.y / groups;
+  const int h_first = kvh * p.g + (blockIdx.y % groups) * G;  // first query head of this CTA
+  const int blk_lo = split * p.blocks_per_split;
+  const int blk_hi = min(p.nblk, blk_lo + p.blocks_per_split);
+  const int nb = max(0, blk_hi - blk_lo);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::PRODUCER_WARP) {
+    if (lane == 0 && nb > 0) {
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < nb; ++i) {
+        const int slot = i % C::STAGES, use = i / C::STAGES;
+        if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.status, kSiteDecEmpty)) break;
+        uint8_t* st = smem + slot * C::STAGE_BYTES;
+        const int row = (blk_lo + i) * kDecBN;
+        mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+        tma_load_4d_hint(st, &p.tm_k, &full[slot], 0, kvh, row, bi, pol);
+        tma_load_4d_hint(st + C::KV_BYTES, &p.tm_v, &full[slot], 0, kvh, row, bi, pol);
+        ++issued;
+      }
+      for (int i = max(0, issued - C::STAGES); i < issued; ++i)
+        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, p.status, kSiteDecDrain)) break;
+    }
+    __syncwarp();
+    __syncthreads();
+    return;
+  }
+
+  // ------------------------------ compute warps ------------------------------
+  const int c = lane % L::LPR;      // dim group of this lane
+  const int rg = lane / L::LPR;     // row within a pass
+  // dims owned: segment s covers [s * D / SEG + 8 c, + 8)
+  float q[G][L::DPL];
+  float acc[G][L::DPL];
+  float m[G], l[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int hq = h_first + h;
+    const void* qrow = static_cast<const uint8_t*>(p.q) + 2 * (bi * p.q_stride_b + hq * p.q_stride_h);
+#pragma unroll
+    for (int s = 0; s < L::SEG; ++s)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        q[h][8 * s + e] = load_elem<BF16>(qrow, s * (D / L::SEG) + 8 * c + e) * p.scale_log2;
+        acc[h][8 * s + e] = 0.f;
+      }
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+
+  bool ok = true;
+  for (int i = 0; i < nb; ++i) {
+    const int slot = i % C::STAGES;
+    // warp-uniform outcome: the shuffles below need every lane
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (i / C::STAGES) & 1, p.status, kSiteDecFull))) {
+      ok = false;
+      break;
+    }
+    const uint8_t* ks = smem + slot * C::STAGE_BYTES;
+    const uint8_t* vs = ks + C::KV_BYTES;
+    const int key0 = (blk_lo + i) * kDecBN + warp * kDecRowsPerWarp;
+    // scores (log2 domain, scale folded into q) for this lane's row in each pass
+    float sc[L::PASSES][G];
+#pragma unroll
+    for (int ps = 0; ps < L::PASSES; ++ps) {
+      const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+      float kf[L::DPL];
+#pragma unroll
+      for (int s = 0; s < L::SEG; ++s) {
+        const uint4 u = *reinterpret_cast<const uint4*>(ks + kr * (D * 2) + 2 * (s * (D / L::SEG) + 8 * c));
+        unpack8<BF16>(u, kf + 8 * s);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < L::DPL; ++e) a = fmaf(q[h][e], kf[e], a);
+        sc[ps][h] = a;
+      }
+#pragma unroll
+      for (int x = 1; x < L::LPR; x <<= 1)
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[ps][h] += __shfl_xor_sync(0xffffffffu, sc[ps][h], x);
+      const int key = key0 + ps * L::RPP + rg;
+      if (key >= p.kv_limit) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[ps][h] = -INFINITY;
+      }
+    }
+    // block max per head over this warp's rows
+    float mn[G], alpha[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float bm = sc[0][h];
+#pragma unroll
+      for (int ps = 1; ps < L::PASSES; ++ps) bm = fmaxf(bm, sc[ps][h]);
+#pragma unroll
+      for (int x = L::LPR; x < 32; x <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, x));
+      mn[h] = fmaxf(m[h], bm);
+      const float mu = (mn[h] == -INFINITY) ? 0.f : mn[h];
+      alpha[h] = ex2_approx(m[h] - mu);
+      m[h] = mn[h];
+      mn[h] = mu;
+    }
+    // probabilities, running sums, rescale and accumulate P V
+    float ps_sum[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      ps_sum[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < L::DPL; ++e) acc[h][e] *= alpha[h];
+    }
+#pragma unroll
+    for (int ps = 0; ps < L::PASSES; ++ps) {
+      const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+      float vf[L::DPL];
+#pragma unroll
+      for (int s = 0; s < L::SEG; ++s) {
+        const uint4 u = *reinterpret_cast<const uint4*>(vs + kr * (D * 2) + 2 * (s * (D / L::SEG) + 8 * c));
+        unpack8<BF16>(u, vf + 8 * s);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pr = ex2_approx(sc[ps][h] - mn[h]);
+        ps_sum[h] += pr;
+#pragma unroll
+        for (int e = 0; e < L::DPL; ++e) acc[h][e] = fmaf(pr, vf[e], acc[h][e]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float sgl = ps_sum[h];
+#pragma unroll
+      for (int x = L::LPR; x < 32; x <<= 1) sgl += __shfl_xor_sync(0xffffffffu, sgl, x);
+      l[h] = alpha[h] * l[h] + sgl;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+
+  // ---- merge the lanes that handled different rows (same dims) ----
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < L::DPL; ++e)
+#pragma unroll
+      for (int x = L::LPR; x < 32; x <<= 1) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], x);
+  // ---- merge the four warps through shared memory ----
+  float* my = red + warp * G * (D + 2);
+  if (rg == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int s = 0; s < L::SEG; ++s)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) my[h * (D + 2) + s * (D / L::SEG) + 8 * c + e] = acc[h][8 * s + e];
+      if (c == 0) {
+        my[h * (D + 2) + D] = m[h];
+        my[h * (D + 2) + D + 1] = l[h];
+      }
+    }
+  }
+  // all compute threads (and the producer) meet here
+  __syncthreads();
+  if (!ok) return;
+  const int nthreads = kDecWarps * 32;
+  for (int idx = threadIdx.x; idx < G * D; idx += nthreads) {
+    const int h = idx / D, e = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
+    float Lsum = 0.f, o = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float f = ex2_approx(red[(w * G + h) * (D + 2) + D] - M);
+        Lsum += f * red[(w * G + h) * (D + 2) + D + 1];
+        o += f * red[(w * G + h) * (D + 2) + e];
+      }
+    }
+    const int hq = h_first + h;
+    const int64_t prow = (static_cast<int64_t>(split) * p.b + bi) * p.hq + hq;  // sq == 1
+    p.o_part[prow * D + e] = Lsum > 0.f ? o / Lsum : 0.f;
+    if (e == 0) p.lse_part[prow] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
+  }
+}
+
+template <int D, int G, bool BF16>
+cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  auto kern = fa_decode_kernel<D, G, BF16>;
+  const int smem = C::STAGES * C::STAGE_BYTES + 2 * C::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 128;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_splits, p.hkv * (p.g / G), p.b);
+  kern<<<grid, C::THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int G, bool BF16>
+int dec_occupancy() {
+  using C = DecCfg<D>;
+  const int smem = C::STAGES * C::STAGE_BYTES + 2 * C::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 128;
+  auto kern = fa_decode_kernel<D, G, BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_dec_g(const DecodeParams& p, cudaStream_t stream) {
+  switch (decode_heads_per_cta(p.g)) {
+    case 1: return launch_dec<D, 1, BF16>(p, stream);
+    case 2: return launch_dec<D, 2, BF16>(p, stream);
+    default: return launch_dec<D, 4, BF16>(p, stream);
+  }
+}
+
+// ------------------------------------------------------------------ combine
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_combine_kernel(const __grid_constant__ CombineParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nrows = static_cast<int64_t>(p.b) * p.hq * p.sq;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= nrows) return;
+  const int i = static_cast<int>(row % p.sq);
+  const int h = static_cast<int>((row / p.sq) % p.hq);
+  const int bi = static_cast<int>(row / (static_cast<int64_t>(p.sq) * p.hq));
+  constexpr float kLog2e = 1.4426950408889634f;
+  // LSE_total = logsumexp over splits
+  float M = -INFINITY;
+  for (int s = lane; s < p.num_splits; s += 32) M = fmaxf(M, p.lse_part[s * nrows + row]);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+  uint16_t* orow = static_cast<uint16_t*>(p.o) + bi * p.o_stride_b + static_cast<int64_t>(i) * p.o_stride_row +
+                   h * p.o_stride_h;
+  if (M == -INFINITY) {
+    for (int e = lane; e < p.d; e += 32) orow[e] = 0;
+    if (lane == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
+    return;
+  }
+  float ssum = 0.f;
+  for (int s = lane; s < p.num_splits; s += 32) ssum += ex2_approx((p.lse_part[s * nrows + row] - M) * kLog2e);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, x);
+  const float lse = M + lg2_approx(ssum) * kLn2;
+  // O = sum_s e^(LSE_s - LSE) O_s; lanes own dims e = lane + 32 k (k < 8, d <= 256)
+  float o[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) o[k] = 0.f;
+  for (int s = 0; s < p.num_splits; ++s) {
+    const float ls = p.lse_part[s * nrows + row];
+    if (ls == -INFINITY) continue;
+    const float w = ex2_approx((ls - lse) * kLog2e);
+    const float* op = p.o_part + (s * nrows + row) * p.d;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = lane + 32 * k;
+      if (e < p.d) o[k] = fmaf(w, op[e], o[k]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = lane + 32 * k;
+    if (e < p.d) {
+      if constexpr (BF16) {
+        orow[e] = __bfloat16_as_ushort(__float2bfloat16_rn(o[k]));
+      } else {
+        orow[e] = __half_as_ushort(__float2half_rn(o[k]));
+      }
+    }
+  }
+  if (lane == 0 && p.lse != nullptr) p.lse[row] = lse;
+}
+
+// ------------------------------------------------------------------ self test
+// A wait that nothing completes: it must give up after the limit, record the
+// timeout in the status word and return.
+__global__ void fa_wait_selftest_kernel(int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, status, 0x7f);
+  __syncthreads();
+}
+
+}  // namespace
+
+int decode_block_n(int) { return kDecBN; }
+
+int decode_heads_per_cta(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
+
+bool decode_supported(int d, int g) { return (d == 64 || d == 128 || d == 256) && g >= 1; }
+
+int decode_ctas_per_sm(int d, int dtype) {
+  const bool bf16 = dtype == 0;
+  switch (d) {
+    case 64: return bf16 ? dec_occupancy<64, 4, true>() : dec_occupancy<64, 4, false>();
+    case 128: return bf16 ? dec_occupancy<128, 4, true>() : dec_occupancy<128, 4, false>();
+    case 256: return bf16 ? dec_occupancy<256, 4, true>() : dec_occupancy<256, 4, false>();
+    default: return 1;
+  }
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int d, int dtype, cudaStream_t stream) {
+  const bool bf16 = dtype == 0;
+  switch (d) {
+    case 64: return bf16 ? launch_dec_g<64, true>(p, stream) : launch_dec_g<64, false>(p, stream);
+    case 128: return bf16 ? launch_dec_g<128, true>(p, stream) : launch_dec_g<128, false>(p, stream);
+    case 256: return bf16 ? launch_dec_g<256, true>(p, stream) : launch_dec_g<256, false>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_combine(const CombineParams& p, int dtype, cudaStream_t stream) {
+  const int64_t nrows = static_cast<int64_t>(p.b) * p.hq * p.sq;
+  if (nrows == 0) return cudaSuccess;
+  const int64_t blocks = (nrows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (dtype == 0)
+    fa_combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  else
+    fa_combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream) {
+  fa_wait_selftest_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

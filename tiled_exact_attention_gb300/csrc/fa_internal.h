@@ -1,0 +1,72 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Parameters of the prefill / split kernels (passed by value as a grid constant).
+struct PrefillParams {
+  CUtensorMap tm_q;  // Q  [b][sq][hq][d],  box {64, 1, 128, 1}
+  CUtensorMap tm_k;  // K  [b][skv][hkv][d], box {64, 1, BN, 1}
+  CUtensorMap tm_v;  // V  same as K
+  CUtensorMap tm_o;  // O  same as Q (unused in split mode)
+  void* o;           // O base (empty tiles are written directly)
+  float* lse;        // LSE [b][hq][sq] (or LSE partials [ns][b][hq][sq] in split mode)
+  float* o_part;     // split mode: normalised partial outputs [ns][b][hq][sq][d]
+  int64_t o_stride_b, o_stride_row, o_stride_h;  // elements
+  int b, sq, skv, hq, hkv, g;
+  int causal;
+  int off;             // row i sees key j iff j <= i + off (when causal)
+  float scale_log2;    // scale * log2(e)
+  int n_mtiles;        // ceil(sq / 128)
+  int n_mcta;          // ceil(n_mtiles / NQ)
+  int num_splits;      // 1 = plain forward
+  int blocks_per_split;
+  int* status;
+};
+
+// Parameters of the CUDA-core split-KV decode kernel (sq == 1).
+struct DecodeParams {
+  CUtensorMap tm_k;  // K [b][skv][hkv][d], box {d, 1, BN, 1}, no swizzle
+  CUtensorMap tm_v;
+  const void* q;     // Q [b][1][hq][d]
+  int64_t q_stride_b, q_stride_h;
+  float* o_part;     // [ns][b][hq][1][d]
+  float* lse_part;   // [ns][b][hq][1]
+  int b, skv, hq, hkv, g;
+  int nblk;          // ceil(skv / BN)
+  int blocks_per_split;
+  int num_splits;
+  int kv_limit;      // keys j < kv_limit are visible (min(skv, off + 1) when causal)
+  float scale_log2;
+  int* status;
+};
+
+struct CombineParams {
+  const float* o_part;   // [ns][b][hq][sq][d]
+  const float* lse_part; // [ns][b][hq][sq]
+  void* o;
+  int64_t o_stride_b, o_stride_row, o_stride_h;
+  float* lse;            // [b][hq][sq] (may be null)
+  int num_splits, b, hq, sq, d;
+};
+
+// Launchers: return cudaSuccess or the launch error.  `dtype` 0 = bf16, 1 = fp16.
+cudaError_t launch_prefill(const PrefillParams& p, int d, int dtype, cudaStream_t stream);
+int prefill_block_n(int d);   // keys per KV block of the prefill kernel
+int prefill_q_tiles(int d);   // 128-row Q tiles per CTA
+
+cudaError_t launch_decode(const DecodeParams& p, int d, int dtype, cudaStream_t stream);
+int decode_block_n(int d);
+int decode_ctas_per_sm(int d, int dtype);
+int decode_heads_per_cta(int g);  // query heads of one KV group handled by one CTA
+bool decode_supported(int d, int g);
+
+cudaError_t launch_combine(const CombineParams& p, int dtype, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
+
+}  // namespace fa
