@@ -1,0 +1,450 @@
+"""Benchmark of the tiled exact attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * causal prefill forward (fa_fwd) on B=4, Hq=Hkv=16, N=4096, d=128, bf16;
+  * split-KV decode (fa_fwd_splitkv: split kernel + LSE-weighted combine) on
+    B=8, Hq=32, Hkv=8, KV length 32768, d=128, bf16, query position 32767.
+`value` is the prefill's forward TFLOP/s (4 * d * visible (query, key) pairs *
+b * hq per launch, over that launch's CUDA-event time); the decode's KV GB/s is
+reported beside it.  L2 is flushed (a 256 MiB write) before every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload.  With N > 1 (torchrun) every rank runs an
+independent replica; the line reports the total over ranks and the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd TFLOP/s & % bf16 tensor peak (prefill); decode KV GB/s & % HBM BW"
+PREFILL = "causal_prefill"
+DECODE = "decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("fa_prefill.cu", "fa_decode.cu", "ptx.cuh", "fa_internal.h"):
+        with open(os.path.join(ROOT, "tiled_exact_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    want = _kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.strip().strip("|").split("|")
+            parts = [x.strip() for x in parts]
+            if len(parts) >= 3 and parts[0] == kernel and parts[1] == want:
+                try:
+                    return int(float(parts[2]))
+                except ValueError:
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.5)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sms, maxs, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        sms_sorted = sorted(sms)
+        med = sms_sorted[len(sms_sorted) // 2] if sms_sorted else None
+        return {"sm_mhz": med, "sm_max_mhz": max(maxs) if maxs else None, "reasons": sorted(reasons),
+                "samples": len(sms), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------- our implementation
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from tiled_exact_attention_gb300 import fa_fwd, fa_fwd_splitkv, fa_splitkv_default_splits, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    __graft_entry__.build()
+
+    wp, wd = WORKLOADS[PREFILL], WORKLOADS[DECODE]
+    qc, kc, vc = make_qkv(wp)
+    q, k, v = qc.to(dev), kc.to(dev), vc.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((wp.b, wp.hq, wp.sq), dtype=torch.float32, device=dev)
+    dqc, dkc, dvc = make_qkv(wd)
+    dq, dk, dv = dqc.to(dev), dkc.to(dev), dvc.to(dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty((wd.b, wd.hq, wd.sq), dtype=torch.float32, device=dev)
+    ns = fa_splitkv_default_splits(dq, dk, dv, causal=True, q_pos_offset=wd.offset)
+    from tiled_exact_attention_gb300.api import fa_splitkv_workspace_size
+
+    wsb = fa_splitkv_workspace_size(dq, dk, dv, ns, causal=True, q_pos_offset=wd.offset)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        fa_fwd(q, k, v, causal=True, q_pos_offset=wp.offset, out=o, lse=lse)
+
+    def decode():
+        fa_fwd_splitkv(dq, dk, dv, causal=True, q_pos_offset=wd.offset, num_splits=ns, workspace=work, out=do,
+                       lse=dlse)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill()
+        decode()
+    st = fa_sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        prefill()
+        evs[i][1].record(stream)
+        decode()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    st = fa_sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+    pre_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    dec_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    pre_avg = sum(pre_ms) / K
+    dec_avg = sum(dec_ms) / K
+    step_ms = pre_avg + dec_avg
+
+    # ---- end-to-end through the public call with host buffers (prefill) ----
+    hq_, hk_, hv_ = (t.pin_memory() for t in (qc, kc, vc))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(3, min(50, K // 20))
+    for _ in range(2):
+        q.copy_(hq_, non_blocking=True), k.copy_(hk_, non_blocking=True), v.copy_(hv_, non_blocking=True)
+        prefill()
+        ho.copy_(o, non_blocking=True), hl.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        flush.zero_()
+        q.copy_(hq_, non_blocking=True)
+        k.copy_(hk_, non_blocking=True)
+        v.copy_(hv_, non_blocking=True)
+        prefill()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
+    kv_bytes = 2 * wd.b * wd.hkv * wd.skv * wd.d * 2
+    dec_bytes = kv_bytes + 2 * (wd.b * wd.hq * wd.d * 2) + wd.b * wd.hq * 4
+
+    if ws > 1:
+        t = torch.tensor([pre_avg, dec_avg, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        pre_avg, dec_avg, e2e_ms = (float(x) for x in t.tolist())
+        step_ms = pre_avg + dec_avg
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = _peaks()
+    tflops = flops * ws / (pre_avg * 1e-3) / 1e12
+    per_gpu_tflops = flops / (pre_avg * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (dec_avg * 1e-3) / 1e9
+    pk = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    pk_burst = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    h2d = sum(t.numel() * t.element_size() for t in (qc, kc, vc))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    pre_traffic = _profiled_traffic("fa_prefill_kernel")
+    dec_traffic = _profiled_traffic("fa_decode_kernel")
+    line = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: iid N(0,1) bf16 from seeded PCG64, no dataset",
+        "config": {
+            "workload": "causal prefill B=4 Hq=Hkv=16 N=4096 d=128 bf16 + split-KV decode B=8 Hq=32 Hkv=8 "
+                        "KV=32768 d=128 bf16 (query position 32767)",
+            "prefill": {"b": wp.b, "sq": wp.sq, "skv": wp.skv, "hq": wp.hq, "hkv": wp.hkv, "d": wp.d,
+                        "causal": True, "flops_per_launch": flops, "ms": round(pre_avg, 4)},
+            "decode": {"b": wd.b, "skv": wd.skv, "hq": wd.hq, "hkv": wd.hkv, "d": wd.d, "num_splits": ns,
+                       "bytes_per_launch": dec_bytes, "ms": round(dec_avg, 4)},
+            "l2": "flushed before every step (256 MiB write, outside the kernel events)",
+            "parallelism": f"replicas x{ws} (independent problems per GPU)",
+            "timing": "CUDA events per phase on the launching stream, mean over the timed steps",
+        },
+        "decode": {
+            "value": round(dec_gbs, 1),
+            "unit": "GB/s",
+            "ms_per_step": round(dec_avg, 4),
+            "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(dec_gbs / hbm, 4), "peak_source": peak_src,
+                         "traffic": dec_traffic, "spec_peak": 8000.0,
+                         "frac_of_spec": round(dec_gbs / 8000.0, 4),
+                         "note": "phase time = split kernel + combine kernel"},
+        },
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
+                     "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
+                     "kernel": "fa_prefill_kernel<128, bf16>",
+                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
+                     "frac_of_burst": round(per_gpu_tflops / pk_burst, 4), "spec_peak": 2250.0,
+                     "frac_of_spec": round(per_gpu_tflops / 2250.0, 4)},
+        "clocks": clocks,
+        "e2e": {"value": round(flops * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step"},
+        "gpu_launches": K * 3,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------- oracle (CPU) arm
+
+
+def _sample_rows(w, n_rows, seed):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(w.b * w.hq * w.sq, size=min(n_rows, w.b * w.hq * w.sq), replace=False)
+    bi = idx // (w.hq * w.sq)
+    hi = (idx // w.sq) % w.hq
+    ii = idx % w.sq
+    return np.stack([bi, hi, ii], axis=1).astype(np.int64)
+
+
+def _pairs(w, rows):
+    import numpy as np
+
+    if not w.causal:
+        return int(rows.shape[0]) * w.skv
+    return int(np.clip(rows[:, 2] + w.offset + 1, 0, w.skv).sum())
+
+
+def cpu_baseline(budget_s=15.0, seed=1):
+    """Time the oracle as it stands on the host cores over a random sample of the
+    prefill workload's rows; report the algorithmic TFLOP/s of that sample."""
+    import numpy as np
+
+    import oracle
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+
+    w = WORKLOADS[PREFILL]
+    qc, kc, vc = make_qkv(w)
+    q, k, v = (t.to(__import__("torch").float64).numpy() for t in (qc, kc, vc))
+    # calibrate on a small sample, then size the sample for the budget
+    rows = _sample_rows(w, 256, seed)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
+    t_small = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(w.b * w.hq * w.sq, max(256, 256 * budget_s / t_small)))
+    rows = _sample_rows(w, n, seed + 1)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.d * _pairs(w, rows)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} random query rows of the causal prefill workload (all heads/batches), "
+                      f"{_pairs(w, rows)} visible pairs, {dt:.2f} s, fp64 C oracle with OpenMP",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+
+    w = WORKLOADS[PREFILL]
+    qc, kc, vc = make_qkv(w)
+    import torch
+
+    q, k, v = (t.to(torch.float64).numpy() for t in (qc, kc, vc))
+    total_budget = 90.0
+    rows = _sample_rows(w, 128, 7)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
+    t_small = max(time.perf_counter() - t0, 1e-3)
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    n = int(min(w.b * w.hq * w.sq, max(16, 128 * per_step / t_small)))
+    for i in range(args.warmup):
+        oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=_sample_rows(w, n, 100 + i))
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        rows = _sample_rows(w, n, 1000 + i)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
+        times.append(time.perf_counter() - t0)
+        flops += 4.0 * w.d * _pairs(w, rows)
+    tt = sum(times)
+    val = flops / tt / 1e12
+    sample = f"{n} random query rows per step of the causal prefill workload, fp64 C oracle with OpenMP"
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tt / max(1, args.steps), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: iid N(0,1) bf16 from seeded PCG64, converted exactly to fp64",
+        "config": {"workload": "causal prefill B=4 Hq=Hkv=16 N=4096 d=128 (bounded row sample per step)"},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -28,6 +28,7 @@ namespace fa {
 namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 
 template <int D>
 struct Cfg {
@@ -125,7 +126,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- which tiles this CTA owns (heaviest causal row-groups first) ----
+  // ---- which tiles this CTA owns ----
+  // Longest causal row-groups first over the whole grid (longest-processing-time
+  // order balances the SMs best; grouping CTAs by head measured slower).
   int idx = blockIdx.x;
   const int split = idx % p.num_splits;
   idx /= p.num_splits;
@@ -335,9 +338,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
       const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m_run, bmax * sl2);
+      // The reference max moves only when the block max exceeds it by more than
+      // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
+      // unchanged); probabilities stay below 2^kRescaleLog2.
+      const float bm2 = bmax * sl2;
+      const bool grow = bm2 > m_run + kRescaleLog2;
+      const float m_new = grow ? bm2 : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_use);
+      const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
       float sum[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum[i] = 0.f;
@@ -355,24 +363,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       l_run = alpha * l_run + rs;
       m_run = m_new;
       tmem_st_wait();
-      if (k > 0) {
+      if (k > 0 && __any_sync(0xffffffffu, grow)) {
         // O_t must hold the previous block's product before it is rescaled.
         if (!warp_wait(&o_full[t], (k - 1) & 1, p.status, kSiteOFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        constexpr int CH = D < 128 ? D : 128;
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_load_row<32>(tO + c, o);
+        for (int c0 = 0; c0 < D; c0 += CH) {
+          uint32_t o[CH];
+          tmem_load_row<CH>(tO + c0, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < CH; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+#pragma unroll
+          for (int c = 0; c < CH; c += 32) tmem_st32(tO + c0 + c, *reinterpret_cast<const uint32_t(*)[32]>(o + c));
         }
+        tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(&p_full[t]);
