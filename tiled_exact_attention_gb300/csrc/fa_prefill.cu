@@ -39,7 +39,9 @@ struct Cfg {
   static constexpr int DC = D / 64;                  // 64-column (128-byte) chunks
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NUM_WARPS = 4 * NQ + 2;
+  // softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle
+  // warps) so that register budgets can be moved between whole warpgroups
+  static constexpr int NUM_WARPS = 4 * NQ + 4;
   static constexpr int THREADS = 32 * NUM_WARPS;
   static constexpr int PRODUCER_WARP = 4 * NQ;
   static constexpr int MMA_WARP = 4 * NQ + 1;
@@ -49,6 +51,12 @@ struct Cfg {
   static constexpr int BAR_OFF = RING_OFF + STAGES * KV_BYTES;
   static constexpr int NUM_BARS = 4 * NQ + 2 * STAGES;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;
+  // Register split (NQ == 2): launched at 168 per thread (384 threads), the
+  // control warpgroup drops to 72 and the two softmax warpgroups rise to 216:
+  // 2 * 128 * 216 + 128 * 72 = 384 * 168.
+  static constexpr int REG_SOFTMAX = 216;
+  static constexpr int REG_CONTROL = 72;
+  static_assert(NQ == 1 || 2 * 128 * REG_SOFTMAX + 128 * REG_CONTROL <= THREADS * 168, "register split");
   static_assert(NQ * BN <= 256, "S buffers must fit below the O columns");
   static_assert(O_COL0 + NQ * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -66,6 +74,12 @@ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b :
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int site) {
   const bool ok = mbar_wait(bar, parity, status, site);
   return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 template <int N>
@@ -104,6 +118,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// S_t = Q_t K^T over the head dimension: D / 16 MMAs of K = 16, both operands
+// K-major with 128-byte swizzle (64-column chunks of 128-byte rows).
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID>
+__device__ __forceinline__ void issue_s_tile(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int t, int slot) {
+  const uint64_t qd = q_desc + static_cast<uint32_t>((t * Q_BYTES) >> 4);
+  const uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
+    const uint32_t offb = static_cast<uint32_t>(((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4);
+    umma_ss(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t[:, 16 k0 : 16 k1] V[16 k0 : 16 k1, :]: P from TMEM (two 16-bit
+// values per column), V MN-major with 128-byte swizzle (64-column atoms BN * 128
+// bytes apart, 8-row groups 1024 bytes apart).
+template <int D, int BN, int KV_BYTES, uint32_t ID, int K0, int K1>
+__device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, int slot, bool acc) {
+  const uint64_t vd = v_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+#pragma unroll
+  for (int k = K0; k < K1; ++k) {
+    umma_ts(o_tmem, p_tmem + k * 8, vd + static_cast<uint32_t>((k * 2048) >> 4), ID, (acc || k > 0) ? 1u : 0u);
   }
 }
 
@@ -186,6 +226,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= 4 * NQ) {
+    // Control warpgroup: each register budget covers only its own role's code.
+    if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_CONTROL));
   if (warp == C::PRODUCER_WARP) {
     // =========================== TMA producer ===========================
     if (lane == 0 && N > 0) {
@@ -229,27 +272,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     if (lane == 0 && N > 0) {
       constexpr uint32_t kIdS = idesc_f16(BM, BN, BF16, false);
       constexpr uint32_t kIdO = idesc_f16(BM, D, BF16, true);
+      // Descriptors are built once; per slot, tile and K step only the start
+      // address field (low bits, address >> 4) moves, by compile-time amounts.
       const uint32_t ring_s = smem_u32(ring);
-      const uint32_t q_s = smem_u32(smem);
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = q_s + t * C::Q_BYTES;
-        const uint32_t ka = ring_s + slot * C::KV_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off_a = (k >> 2) * (BM * 128) + (k & 3) * 32;
-          const uint32_t off_b = (k >> 2) * (BN * 128) + (k & 3) * 32;
-          umma_ss(tbase + Cfg<D>::s_col(t), sdesc_sw128(qa + off_a, 16, 1024), sdesc_sw128(ka + off_b, 16, 1024),
-                  kIdS, k > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t va = ring_s + slot * C::KV_BYTES;
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          umma_ts(tbase + Cfg<D>::o_col(t), tbase + Cfg<D>::s_col(t) + k * 8,
-                  sdesc_sw128(va + k * 2048, BN * 128, 1024), kIdO, (acc || k > 0) ? 1u : 0u);
-        }
-      };
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);  // Q tile 0, K step 0
+      const uint64_t k_desc = sdesc_sw128(ring_s, 16, 1024);          // slot 0 read as K (K-major)
+      const uint64_t v_desc = sdesc_sw128(ring_s, BN * 128, 1024);    // slot 0 read as V (MN-major)
       auto active = [&](int t, int it) { return n_hi_max - 1 - it < n_hi[t]; };
       bool ok = true;
 #pragma unroll
@@ -263,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
           if (active(t, 0)) {
-            issue_s(t, 0);
+            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t, 0);
             umma_commit(&s_full[t]);
           }
         umma_commit(&kv_empty[0]);
@@ -272,22 +300,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         const int Lv = 2 * it + 1, Lk = 2 * it + 2;
         const bool has_next = it + 1 < N;
         if (!mbar_wait(&kv_full[Lv % C::STAGES], (Lv / C::STAGES) & 1, p.status, kSiteKvFull)) break;
-        if (has_next && !mbar_wait(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) break;
         tc_fence_after();
+        bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < NQ; ++t) {
           if (active(t, it)) {
+            // first half of P: start PV while the softmax finishes the second half
             if (!mbar_wait(&p_full[t], pv_count[t] & 1, p.status, kSitePFull)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_pv(t, Lv % C::STAGES, pv_count[t] > 0);
+            issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 16>(tbase + Cfg<D>::o_col(t),
+                                                               tbase + Cfg<D>::s_col(t), v_desc,
+                                                               Lv % C::STAGES, pv_count[t] > 0);
             umma_commit(&o_full[t]);
             ++pv_count[t];
           }
           if (has_next && active(t, it + 1)) {
-            issue_s(t, Lk % C::STAGES);
+            if (!k_ready) {
+              if (!mbar_wait(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
+                                                                   Lk % C::STAGES);
             umma_commit(&s_full[t]);
           }
         }
@@ -297,7 +337,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       }
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     // =========================== softmax warpgroups ===========================
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -321,6 +363,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         break;
       }
       tc_fence_after();
+      if (k > 0) {
+        // S_k complete implies PV_{k-1} complete; observe that phase of o_full so
+        // the final wait below is never more than one phase behind.
+        if (!warp_wait(&o_full[t], (k - 1) & 1, p.status, kSiteOFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       uint32_t sr[BN];
       tmem_load_row<BN>(tS, sr);
       float* s = reinterpret_cast<float*>(sr);
@@ -331,13 +382,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         for (int c = 0; c < BN; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 4; ++i) mx[i] = fmax3(s[2 * i], s[2 * i + 1], s[8 + i]);
 #pragma unroll
-      for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 12; c < BN; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (c + 2 * i + 1 < BN) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        }
+      }
+      const float bmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       // The reference max moves only when the block max exceeds it by more than
       // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
       // unchanged); probabilities stay below 2^kRescaleLog2.
@@ -346,44 +401,56 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       const float m_new = grow ? bm2 : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
-      float sum[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum[i] = 0.f;
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
-        sum[(c >> 1) & 7] += p0 + p1;
-        pk[c >> 1] = pack2<BF16>(p0, p1);
-      }
-      const float rs = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-#pragma unroll
-      for (int c = 0; c < BN / 2; c += 16) tmem_st16(tS + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
-      l_run = alpha * l_run + rs;
-      m_run = m_new;
-      tmem_st_wait();
       if (k > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_t must hold the previous block's product before it is rescaled.
-        if (!warp_wait(&o_full[t], (k - 1) & 1, p.status, kSiteOFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        constexpr int CH = D < 128 ? D : 128;
+        // O_t already holds the previous blocks' product (see the o_full wait).
+        // 32 columns at a time: the 128 scores are still live in registers.
+        constexpr int CH = 32;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += CH) {
           uint32_t o[CH];
           tmem_load_row<CH>(tO + c0, o);
 #pragma unroll
-          for (int i = 0; i < CH; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < CH; i += 2) {
+            const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                        make_float2(alpha, alpha));
+            o[i] = __float_as_uint(r.x);
+            o[i + 1] = __float_as_uint(r.y);
+          }
 #pragma unroll
           for (int c = 0; c < CH; c += 32) tmem_st32(tO + c0 + c, *reinterpret_cast<const uint32_t(*)[32]>(o + c));
         }
-        tmem_st_wait();
       }
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      // P = 2^(s * scale * log2 e - m), written over the first half of the S
+      // columns as packed 16-bit pairs; the MMA warp is signalled once per block
+      // (a second, earlier signal for half of P measured slower).
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-m_use, -m_use);
+      float2 sum2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[BN / 4];
+#pragma unroll
+        for (int c = 0; c < BN / 2; c += 2) {
+          const int cc = half * (BN / 2) + c;
+          const float2 x = __ffma2_rn(make_float2(s[cc], s[cc + 1]), sl2v, negm);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
+          pk[c >> 1] = pack2<BF16>(e.x, e.y);
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 4; c += 16)
+          tmem_st16(tS + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
+        if (half == 1) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_full[t]);
+        }
+      }
+      const float2 s01 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+      l_run = alpha * l_run + (s01.x + s01.y);
+      m_run = m_new;
       ++k;
     }
 
