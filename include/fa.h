@@ -50,7 +50,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, stride or alignment */
   FA_ERR_UNSUPPORTED = 2, /* a head dimension or shape outside the compiled set */
   FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
-  FA_ERR_TIMEOUT = 4      /* a device-side wait gave up (reported by fa_sync_status) */
+  FA_ERR_TIMEOUT = 4,     /* a device-side wait gave up (reported by fa_sync_status) */
+  FA_ERR_SCRATCH_LIMIT = 5 /* fa_fwd_splitkv_noalloc: the problem does not fit the built-in scratch */
 } fa_status;
 
 typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
@@ -145,6 +146,39 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* args, int32_t num_splits, void* work
 fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t b,
                              int32_t hq, int32_t sq, int32_t d, fa_dtype dtype, void* o,
                              const int64_t o_strides[3], float* lse, void* stream);
+
+/* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
+#define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * fa_fwd_splitkv without a caller-supplied workspace (no counterpart in the
+ * reference pages; an addition of this library).
+ *
+ * Some callers cannot allocate device memory for a workspace: a framework
+ * whose memory manager owns the whole device and hands an operator only its
+ * input and output buffers, a plugin interface that passes tensors but no
+ * allocator, or a latency-critical path where cudaMalloc (and the device
+ * synchronisation it may imply) is not acceptable.  This entry point runs
+ * the same split-KV kernels and combine as fa_fwd_splitkv, with the split
+ * partials kept in a fixed buffer compiled into the library: a file-scope
+ * device array of FA_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU which loads
+ * the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   args, num_splits, splits_used, stream: as for fa_fwd_splitkv.
+ *   Returns FA_ERR_SCRATCH_LIMIT, launching nothing, when the workspace the
+ *   problem needs (fa_splitkv_workspace_size(args, num_splits)) exceeds
+ *   FA_NOALLOC_SCRATCH_BYTES; use fa_fwd_splitkv with your own workspace then.
+ *
+ * The first call on a device looks up the buffer's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one buffer: every call overwrites
+ * the parts it uses before reading them, so nothing carries over between
+ * calls, but calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race on the buffer and must be serialised by the
+ * caller.
+ */
+fa_status fa_fwd_splitkv_noalloc(const fa_fwd_args* args, int32_t num_splits, int32_t* splits_used, void* stream);
 
 /*
  * Synchronise `stream` and report device-side failures on the current device:

@@ -13,6 +13,8 @@ FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_ERR_SCRATCH_LIMIT = 5
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 FA_BF16 = 0
 FA_FP16 = 1
@@ -26,6 +28,7 @@ EXPORTS = (
     "fa_splitkv_default_splits",
     "fa_splitkv_workspace_size",
     "fa_fwd_splitkv",
+    "fa_fwd_splitkv_noalloc",
     "fa_splitkv_combine",
     "fa_sync_status",
     "fa_selftest_wait_timeout",
@@ -93,6 +96,8 @@ def load():
         lib.fa_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv.argtypes = [pargs, i32, vp, ctypes.c_size_t, ctypes.POINTER(i32), vp]
         lib.fa_fwd_splitkv.restype = ctypes.c_int
+        lib.fa_fwd_splitkv_noalloc.argtypes = [pargs, i32, ctypes.POINTER(i32), vp]
+        lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

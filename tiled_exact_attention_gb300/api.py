@@ -118,6 +118,20 @@ def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None,
     return out, lse
 
 
+def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None = None,
+                           q_pos_offset: int | None = None, num_splits: int = 0, out=None, lse=None, stream=None,
+                           return_splits=False):
+    """Split-KV forward that uses the library's built-in scratch instead of a workspace."""
+    out, lse = _outputs(q, out, lse)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    used = ctypes.c_int32(0)
+    check(_lib.load().fa_fwd_splitkv_noalloc(ctypes.byref(a), int(num_splits), ctypes.byref(used),
+                                             _stream_handle(stream)), "fa_fwd_splitkv_noalloc")
+    if return_splits:
+        return out, lse, int(used.value)
+    return out, lse
+
+
 def fa_splitkv_combine(o_part, lse_part, out, lse=None, stream=None):
     """Merge fp32 partials o_part [ns, b, hq, sq, d], lse_part [ns, b, hq, sq] into out [b, sq, hq, d]."""
     ns, b, hq, sq, d = o_part.shape

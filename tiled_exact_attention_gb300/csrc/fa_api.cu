@@ -16,6 +16,14 @@ namespace {
 // One status word per device: kernels record the first wait that ran out.
 __device__ int g_fa_status;
 
+// Split-KV scratch for callers that cannot allocate device memory
+// (fa_fwd_splitkv_noalloc).  Every device that loads this library holds it
+// until the process exits.  Host code must not use the symbol's address
+// directly (it is a host-side stand-in): the device address comes from
+// cudaGetSymbolAddress, once per device.
+static_assert(FA_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+static __device__ __align__(256) uint8_t g_splitkv_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -164,6 +172,23 @@ bool split_shape(const fa_fwd_args* a, const DeviceInfo& di, SplitShape* s) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Device address of g_splitkv_scratch on the current device, resolved on the
+// first call for that device (with the device current) and cached.
+bool noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_splitkv_scratch) != cudaSuccess || p == nullptr) return false;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return true;
+}
+
 size_t workspace_bytes_for(const fa_fwd_args* a, int ns) {
   const size_t rows = static_cast<size_t>(ns) * a->b * a->hq * a->sq;
   return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
@@ -198,6 +223,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_UNSUPPORTED: return "unsupported shape or head dimension";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "device-side wait timed out";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more split-KV scratch than the built-in buffer holds";
     default: return "unknown status";
   }
 }
@@ -382,6 +408,23 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
   if (splits_used) *splits_used = ns;
   return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, a->sq, a->d, a->dtype, a->o, a->o_strides, a->lse,
                             stream);
+}
+
+fa_status fa_fwd_splitkv_noalloc(const fa_fwd_args* a, int32_t num_splits, int32_t* splits_used, void* stream) {
+  const fa_status v = validate(a);
+  if (v != FA_OK) return v;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (a->sq == 0) {
+    if (splits_used) *splits_used = 0;
+    return FA_OK;
+  }
+  // the same split count and workspace layout fa_fwd_splitkv would use
+  const size_t need = fa_splitkv_workspace_size(a, num_splits);
+  if (need == 0) return FA_ERR_CUDA;
+  if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if (!noalloc_scratch(&scratch)) return FA_ERR_CUDA;
+  return fa_fwd_splitkv(a, num_splits, scratch, FA_NOALLOC_SCRATCH_BYTES, splits_used, stream);
 }
 
 fa_status fa_sync_status(void* stream) {
