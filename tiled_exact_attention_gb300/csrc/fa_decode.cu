@@ -10,9 +10,9 @@
 //  * 7.3: each split writes its normalised partial output and its LSE (-inf for
 //    a split with no visible key) and the combine kernel merges them with
 //    weights e^(LSE_s - LSE).
-// K/V blocks stream through a shared-memory ring filled by TMA; four compute
-// warps each take 16 rows of every block and keep their own running (m, l, o)
-// per head, merged across warps at the end of the split.
+// K/V blocks stream through a shared-memory ring filled by TMA; eight compute
+// warps each take 8 rows of every block and keep their own running (m, l, o)
+// per head (packed f32x2 FMAs), merged across warps at the end of the split.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -24,12 +24,12 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kDecBN = 64;          // keys per stage
-constexpr int kDecWarps = 4;        // compute warps
+constexpr int kDecWarps = 8;        // compute warps
 constexpr int kDecRowsPerWarp = kDecBN / kDecWarps;
 
 template <int D>
 struct DecCfg {
-  static constexpr int STAGES = (D == 256) ? 2 : 3;
+  static constexpr int STAGES = (D == 256) ? 2 : 4;
   static constexpr int KV_BYTES = kDecBN * D * 2;        // one K or V block
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int THREADS = 32 * (kDecWarps + 1);
@@ -175,10 +175,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float a = 0.f;
+        float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < L::DPL; ++e) a = fmaf(q[h][e], kf[e], a);
-        sc[ps][h] = a;
+        for (int e = 0; e < L::DPL; e += 2)
+          a2 = __ffma2_rn(make_float2(q[h][e], q[h][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
+        sc[ps][h] = a2.x + a2.y;
       }
 #pragma unroll
       for (int x = 1; x < L::LPR; x <<= 1)
@@ -211,7 +212,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
     for (int h = 0; h < G; ++h) {
       ps_sum[h] = 0.f;
 #pragma unroll
-      for (int e = 0; e < L::DPL; ++e) acc[h][e] *= alpha[h];
+      for (int e = 0; e < L::DPL; e += 2) {
+        const float2 r = __fmul2_rn(make_float2(acc[h][e], acc[h][e + 1]), make_float2(alpha[h], alpha[h]));
+        acc[h][e] = r.x;
+        acc[h][e + 1] = r.y;
+      }
     }
 #pragma unroll
     for (int ps = 0; ps < L::PASSES; ++ps) {
@@ -227,7 +232,12 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
         const float pr = ex2_approx(sc[ps][h] - mn[h]);
         ps_sum[h] += pr;
 #pragma unroll
-        for (int e = 0; e < L::DPL; ++e) acc[h][e] = fmaf(pr, vf[e], acc[h][e]);
+        for (int e = 0; e < L::DPL; e += 2) {
+          const float2 r = __ffma2_rn(make_float2(pr, pr), make_float2(vf[e], vf[e + 1]),
+                                      make_float2(acc[h][e], acc[h][e + 1]));
+          acc[h][e] = r.x;
+          acc[h][e + 1] = r.y;
+        }
       }
     }
 #pragma unroll
