@@ -80,6 +80,20 @@ def _profiled_traffic(kernel: str):
     return None
 
 
+def reduce_max_over_ranks(values, dist_mod, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the job time)."""
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(units_per_rank: float, world_size: int, ms: float) -> float:
+    """Whole-job units per second: every rank processes `units_per_rank` in at most `ms`."""
+    return units_per_rank * world_size / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
 
@@ -250,9 +264,7 @@ def run_ours(args):
     dec_bytes = kv_bytes + 2 * (wd.b * wd.hq * wd.d * 2) + wd.b * wd.hq * 4
 
     if ws > 1:
-        t = torch.tensor([pre_avg, dec_avg, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pre_avg, dec_avg, e2e_ms = (float(x) for x in t.tolist())
+        pre_avg, dec_avg, e2e_ms = reduce_max_over_ranks([pre_avg, dec_avg, e2e_ms], dist, dev)
         step_ms = pre_avg + dec_avg
     if rank != 0:
         if ws > 1:
@@ -260,7 +272,7 @@ def run_ours(args):
         return
 
     peaks, peak_src = _peaks()
-    tflops = flops * ws / (pre_avg * 1e-3) / 1e12
+    tflops = job_throughput(flops, ws, pre_avg) / 1e12
     per_gpu_tflops = flops / (pre_avg * 1e-3) / 1e12
     dec_gbs = dec_bytes / (dec_avg * 1e-3) / 1e9
     pk = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -311,7 +323,7 @@ def run_ours(args):
                      "frac_of_burst": round(per_gpu_tflops / pk_burst, 4), "spec_peak": 2250.0,
                      "frac_of_spec": round(per_gpu_tflops / 2250.0, 4)},
         "clocks": clocks,
-        "e2e": {"value": round(flops * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_throughput(flops, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step"},
         "gpu_launches": K * 3,
