@@ -259,6 +259,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
+    paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
+
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
     kv_bytes = 2 * wd.b * wd.hkv * wd.skv * wd.d * 2
     dec_bytes = kv_bytes + 2 * (wd.b * wd.hq * wd.d * 2) + wd.b * wd.hq * 4
@@ -316,6 +318,9 @@ def run_ours(args):
                          "frac_of_spec": round(dec_gbs / 8000.0, 4),
                          "note": "phase time = split kernel + combine kernel"},
         },
+        "decode_paged": dict(paged, roofline={"bound": "hbm", "achieved": paged["value"], "peak": hbm,
+                                              "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
+                                              "peak_source": peak_src, "traffic": None}),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
                      "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
                      "kernel": "fa_prefill_kernel<128, bf16>",
@@ -334,6 +339,68 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def bench_paged_decode(dev, flush, steps=200, warmup=5):
+    """Split-KV decode over a paged KV cache: B=8, Hq=32, Hkv=8, d=128, 256-key pages handed out in a
+    shuffled order, per-sequence lengths drawn (seeded) from [16384, 49152]; KV GB/s of the valid keys."""
+    import numpy as np
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_fwd_kvcache, fa_sync_status
+    from tiled_exact_attention_gb300.api import make_kvcache_args
+    from tiled_exact_attention_gb300.inputs import BASE_SEED, normal
+
+    b, hq, hkv, d, ps = 8, 32, 8, 128, 256
+    rng = np.random.default_rng(BASE_SEED + 50)
+    lens = rng.integers(16384, 49153, size=b).astype(np.int32)
+    pages_per = [int((n + ps - 1) // ps) for n in lens]
+    num_pages = sum(pages_per)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.zeros((b, max(pages_per)), dtype=np.int32)
+    nxt = 0
+    for i, npg in enumerate(pages_per):
+        table[i, :npg] = perm[nxt:nxt + npg]
+        nxt += npg
+    q = normal((b, hq, d), BASE_SEED + 50, 0).to(dev)
+    k = normal((num_pages, ps, hkv, d), BASE_SEED + 50, 1).to(dev)
+    v = normal((num_pages, ps, hkv, d), BASE_SEED + 50, 2).to(dev)
+    bt = torch.from_numpy(table).to(dev)
+    sl = torch.from_numpy(lens).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((b, hq), dtype=torch.float32, device=dev)
+    maxlen = int(lens.max())
+    from tiled_exact_attention_gb300 import _lib
+    import ctypes
+
+    a = make_kvcache_args(q, k, v, o, lse, block_table=bt, seqlens_k=sl, max_seqlen_k=maxlen)
+    ws = torch.empty(int(_lib.load().fa_kvcache_workspace_size(ctypes.byref(a), 0)), dtype=torch.uint8, device=dev)
+
+    def step():
+        return fa_fwd_kvcache(q, k, v, block_table=bt, seqlens_k=sl, max_seqlen_k=maxlen, workspace=ws, out=o,
+                              lse=lse, return_splits=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    ns = 0
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        ns = step()[2]
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if fa_sync_status() != 0:
+        raise RuntimeError("device status set by the paged decode")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    nbytes = 2 * int(lens.sum()) * hkv * d * 2 + 2 * b * hq * d * 2 + b * hq * 4
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "config": {"b": b, "hq": hq, "hkv": hkv, "d": d, "page_size": ps, "keys": int(lens.sum()),
+                       "seqlens": [int(x) for x in lens], "num_splits": ns, "pages": "shuffled"},
+            "bytes_per_launch": nbytes, "steps": steps}
 
 
 # ------------------------------------------------------------------------- oracle (CPU) arm

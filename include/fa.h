@@ -147,6 +147,63 @@ fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t
                              int32_t hq, int32_t sq, int32_t d, fa_dtype dtype, void* o,
                              const int64_t o_strides[3], float* lse, void* stream);
 
+/*
+ * Decode against a KV cache: one new query row per sequence attending to all
+ * keys of its own sequence, whose lengths differ.  The pages' KV-cache path
+ * ("ai-reference-codex: forward CUDA kernel", section 8: flash_attn_with_kvcache
+ * forces split-KV and supports a paged block table; "flash attention V2 code
+ * walkthrough", Flash_fwd_params (cu_seqlens as prefix sums, block_table) and
+ * "moving the kv cache": a cache of [num_blocks, block_size, heads, head_dim]
+ * whose row for (sequence, position) is block_table[position / block_size] *
+ * page_stride + (position % block_size) * row_stride + kv_head * head_stride).
+ *
+ * Two layouts of the keys/values:
+ *   paged   (page_size > 0): k, v are [num_pages, page_size, hkv, d]; sequence
+ *           b's position t lives in page block_table[b * block_table_stride +
+ *           t / page_size] at row t % page_size; seqlens_k[b] keys per sequence.
+ *           page_size must be a multiple of 64.
+ *   packed  (page_size == 0): k, v are [total_k, hkv, d] with sequence b at rows
+ *           [cu_seqlens_k[b], cu_seqlens_k[b + 1]); num_pages holds total_k.
+ * The query of sequence b sees every one of its keys (it stands at position
+ * len_b - 1); a sequence with no key gets O = 0, LSE = -inf.  Rows of the
+ * cache beyond a sequence's length are never used, whatever they hold.
+ */
+typedef struct {
+  fa_dtype dtype;
+  int32_t b, hq, hkv, d;          /* hq % hkv == 0; d in {64, 128, 256} */
+  const void* q;                  /* device, [b, hq, d] */
+  int64_t q_strides[2];           /* (batch, head), in elements */
+  const void* k;                  /* device, see above */
+  const void* v;
+  int64_t k_strides[3];           /* (page, row, head) in elements; packed: (unused, row, head) */
+  int64_t v_strides[3];
+  int32_t num_pages;              /* paged: pages in k / v; packed: total_k */
+  int32_t page_size;              /* keys per page (multiple of 64), or 0 for the packed layout */
+  const int32_t* block_table;     /* device, paged: [b, block_table_stride] page indices */
+  int32_t block_table_stride;
+  const int32_t* seqlens_k;       /* device, paged: [b] keys per sequence */
+  const int32_t* cu_seqlens_k;    /* device, packed: [b + 1] prefix sums */
+  int32_t max_seqlen_k;           /* host-side bound of the keys per sequence (used by the split heuristic only) */
+  void* o;                        /* device, [b, hq, d] of dtype */
+  int64_t o_strides[2];           /* (batch, head), in elements */
+  float* lse;                     /* device, fp32 [b, hq] */
+  float scale;
+} fa_kvcache_args;
+
+/* Workspace bytes fa_fwd_kvcache needs for num_splits splits (0 = its default); 0 if invalid. */
+size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits);
+
+/*
+ * Split-KV decode over a paged or packed KV cache (see fa_kvcache_args): the
+ * same split kernel and LSE-weighted combine as fa_fwd_splitkv, with the key
+ * blocks of each sequence addressed through its block table or its prefix sum
+ * and cut into num_splits ranges of that sequence's own length (0 = the
+ * split-count heuristic, applied with max_seqlen_k).  The workspace is caller-owned device memory of at least
+ * fa_kvcache_workspace_size bytes, 256-byte aligned.
+ */
+fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                         int32_t* splits_used, void* stream);
+
 /* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -99,3 +99,41 @@ def test_combine_validation(lib):
     assert lib.fa_splitkv_combine(None, None, 0, 1, 1, 1, 64, 0, None, st, None, None) == 1
     assert lib.fa_splitkv_combine(None, None, 1, 1, 1, 1, 80, 0, None, st, None, None) == 2
     assert lib.fa_splitkv_combine(None, None, 1, 1, 1, 0, 64, 0, None, st, None, None) == 0
+
+
+def _kv_args(**kw):
+    from tiled_exact_attention_gb300._lib import KvcacheArgs
+
+    a = KvcacheArgs()
+    a.dtype, a.b, a.hq, a.hkv, a.d = 0, 2, 8, 2, 128
+    a.q = a.k = a.v = a.o = 4096
+    a.lse = 4096
+    a.q_strides = (ctypes.c_int64 * 2)(8 * 128, 128)
+    a.o_strides = (ctypes.c_int64 * 2)(8 * 128, 128)
+    a.k_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+    a.v_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+    a.num_pages, a.page_size = 16, 256
+    a.block_table = a.seqlens_k = 4096
+    a.block_table_stride = 8
+    a.max_seqlen_k = 1000
+    a.scale = 0.1
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("page_size", 100, 2), ("page_size", -1, 1), ("block_table", 0, 1), ("seqlens_k", 0, 1), ("d", 80, 2),
+    ("hq", 7, 1), ("num_pages", 0, 1), ("max_seqlen_k", -5, 1), ("k", 4100, 1), ("scale", 0.0, 1),
+])
+def test_kvcache_validation(lib, field, value, expect):
+    a = _kv_args(**{field: value})
+    assert lib.fa_fwd_kvcache(ctypes.byref(a), 0, None, 0, None, None) == expect
+    assert lib.fa_kvcache_workspace_size(ctypes.byref(a), 2) == 0
+
+
+def test_kvcache_packed_needs_prefix_sums(lib):
+    a = _kv_args(page_size=0, cu_seqlens_k=0)
+    assert lib.fa_fwd_kvcache(ctypes.byref(a), 1, None, 0, None, None) == 1
+    a = _kv_args(page_size=0, cu_seqlens_k=4096)
+    assert lib.fa_kvcache_workspace_size(ctypes.byref(a), 3) >= 3 * 2 * 8 * (128 + 1) * 4

@@ -29,6 +29,8 @@ EXPORTS = (
     "fa_splitkv_workspace_size",
     "fa_fwd_splitkv",
     "fa_fwd_splitkv_noalloc",
+    "fa_kvcache_workspace_size",
+    "fa_fwd_kvcache",
     "fa_splitkv_combine",
     "fa_sync_status",
     "fa_selftest_wait_timeout",
@@ -59,6 +61,35 @@ class FwdArgs(ctypes.Structure):
         ("o_strides", ctypes.c_int64 * 3),
         ("causal", ctypes.c_int32),
         ("q_pos_offset", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+    ]
+
+
+class KvcacheArgs(ctypes.Structure):
+    """Mirror of `fa_kvcache_args`."""
+
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("b", ctypes.c_int32),
+        ("hq", ctypes.c_int32),
+        ("hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("q_strides", ctypes.c_int64 * 2),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3),
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int32),
+        ("seqlens_k", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("max_seqlen_k", ctypes.c_int32),
+        ("o", ctypes.c_void_p),
+        ("o_strides", ctypes.c_int64 * 2),
+        ("lse", ctypes.c_void_p),
         ("scale", ctypes.c_float),
     ]
 
@@ -98,6 +129,11 @@ def load():
         lib.fa_fwd_splitkv.restype = ctypes.c_int
         lib.fa_fwd_splitkv_noalloc.argtypes = [pargs, i32, ctypes.POINTER(i32), vp]
         lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+        pkv = ctypes.POINTER(KvcacheArgs)
+        lib.fa_kvcache_workspace_size.argtypes = [pkv, i32]
+        lib.fa_kvcache_workspace_size.restype = ctypes.c_size_t
+        lib.fa_fwd_kvcache.argtypes = [pkv, i32, vp, ctypes.c_size_t, ctypes.POINTER(i32), vp]
+        lib.fa_fwd_kvcache.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

@@ -13,7 +13,7 @@ import math
 import torch
 
 from . import _lib
-from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, check
+from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, KvcacheArgs, check
 
 _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
@@ -127,6 +127,77 @@ def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None
     used = ctypes.c_int32(0)
     check(_lib.load().fa_fwd_splitkv_noalloc(ctypes.byref(a), int(num_splits), ctypes.byref(used),
                                              _stream_handle(stream)), "fa_fwd_splitkv_noalloc")
+    if return_splits:
+        return out, lse, int(used.value)
+    return out, lse
+
+
+def make_kvcache_args(q, k, v, o, lse, *, block_table=None, seqlens_k=None, cu_seqlens_k=None,
+                      max_seqlen_k: int = 0, scale: float | None = None) -> KvcacheArgs:
+    """Fill `fa_kvcache_args`.  q, o: [b, hq, d]; paged k/v: [num_pages, page_size, hkv, d] with
+    block_table [b, n] and seqlens_k [b] (int32); packed k/v: [total_k, hkv, d] with cu_seqlens_k [b + 1]."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", o)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in _DT or t.stride(-1) != 1:
+            raise ValueError(f"{name} must be a CUDA bf16/fp16 tensor with a contiguous last dimension")
+    if q.dim() != 3 or o.shape != q.shape:
+        raise ValueError("q and out must be [b, hq, d]")
+    b, hq, d = q.shape
+    a = KvcacheArgs()
+    a.dtype = _DT[q.dtype]
+    a.b, a.hq, a.d = b, hq, d
+    a.q = q.data_ptr()
+    a.q_strides = (ctypes.c_int64 * 2)(q.stride(0), q.stride(1))
+    a.k, a.v = k.data_ptr(), v.data_ptr()
+    if block_table is not None:
+        if k.dim() != 4 or v.shape != k.shape or seqlens_k is None:
+            raise ValueError("paged cache: k, v [num_pages, page_size, hkv, d] and seqlens_k are required")
+        for t in (block_table, seqlens_k):
+            if t.dtype != torch.int32 or not t.is_cuda:
+                raise ValueError("block_table and seqlens_k must be CUDA int32 tensors")
+        a.num_pages, a.page_size, a.hkv = k.shape[0], k.shape[1], k.shape[2]
+        a.k_strides = (ctypes.c_int64 * 3)(k.stride(0), k.stride(1), k.stride(2))
+        a.v_strides = (ctypes.c_int64 * 3)(v.stride(0), v.stride(1), v.stride(2))
+        a.block_table = block_table.data_ptr()
+        a.block_table_stride = block_table.stride(0)
+        a.seqlens_k = seqlens_k.data_ptr()
+    else:
+        if k.dim() != 3 or v.shape != k.shape or cu_seqlens_k is None:
+            raise ValueError("packed keys: k, v [total_k, hkv, d] and cu_seqlens_k are required")
+        if cu_seqlens_k.dtype != torch.int32 or not cu_seqlens_k.is_cuda:
+            raise ValueError("cu_seqlens_k must be a CUDA int32 tensor")
+        a.num_pages, a.page_size, a.hkv = k.shape[0], 0, k.shape[1]
+        a.k_strides = (ctypes.c_int64 * 3)(0, k.stride(0), k.stride(1))
+        a.v_strides = (ctypes.c_int64 * 3)(0, v.stride(0), v.stride(1))
+        a.cu_seqlens_k = cu_seqlens_k.data_ptr()
+    a.max_seqlen_k = int(max_seqlen_k)
+    a.o = o.data_ptr()
+    a.o_strides = (ctypes.c_int64 * 2)(o.stride(0), o.stride(1))
+    a.lse = lse.data_ptr()
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    return a
+
+
+def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=None, max_seqlen_k=None,
+                   scale=None, num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
+                   return_splits=False):
+    """Decode one query row per sequence against a paged or packed KV cache; returns (O [b, hq, d], LSE [b, hq])."""
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    if max_seqlen_k is None:
+        lens = seqlens_k if block_table is not None else (cu_seqlens_k[1:] - cu_seqlens_k[:-1])
+        max_seqlen_k = int(lens.max().item()) if lens.numel() else 0
+    a = make_kvcache_args(q, k, v, out, lse, block_table=block_table, seqlens_k=seqlens_k,
+                          cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, scale=scale)
+    lib = _lib.load()
+    if workspace is None:
+        need = int(lib.fa_kvcache_workspace_size(ctypes.byref(a), int(num_splits)))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    used = ctypes.c_int32(0)
+    check(lib.fa_fwd_kvcache(ctypes.byref(a), int(num_splits), ctypes.c_void_p(workspace.data_ptr()),
+                             workspace.numel() * workspace.element_size(), ctypes.byref(used),
+                             _stream_handle(stream)), "fa_fwd_kvcache")
     if return_splits:
         return out, lse, int(used.value)
     return out, lse

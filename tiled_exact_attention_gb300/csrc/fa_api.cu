@@ -196,6 +196,51 @@ size_t workspace_bytes_for(const fa_fwd_args* a, int ns) {
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+bool strides_pos(const int64_t* s, int n) {
+  for (int i = 0; i < n; ++i)
+    if (s[i] <= 0) return false;
+  return true;
+}
+
+fa_status validate_kvcache(const fa_kvcache_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
+  if (a->max_seqlen_k < 0 || a->max_seqlen_k > (1 << 30) || a->num_pages < 1) return FA_ERR_INVALID_ARG;
+  if (a->q == nullptr || a->k == nullptr || a->v == nullptr || a->o == nullptr || a->lse == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 2) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 2) || !aligned(a->lse, 4))
+    return FA_ERR_INVALID_ARG;
+  if (!strides_pos(a->q_strides, 2) || !strides_pos(a->o_strides, 2)) return FA_ERR_INVALID_ARG;
+  if (a->page_size > 0) {
+    if (a->page_size % decode_block_n(a->d) != 0) return FA_ERR_UNSUPPORTED;
+    if (a->block_table == nullptr || a->seqlens_k == nullptr || a->block_table_stride < 1) return FA_ERR_INVALID_ARG;
+    if (!aligned(a->block_table, 4) || !aligned(a->seqlens_k, 4)) return FA_ERR_INVALID_ARG;
+    if (!strides_ok(a->k_strides) || !strides_ok(a->v_strides)) return FA_ERR_INVALID_ARG;
+  } else if (a->page_size == 0) {
+    if (a->cu_seqlens_k == nullptr || !aligned(a->cu_seqlens_k, 4)) return FA_ERR_INVALID_ARG;
+    for (int i = 1; i < 3; ++i)
+      if (a->k_strides[i] <= 0 || a->k_strides[i] % 8 != 0 || a->v_strides[i] <= 0 || a->v_strides[i] % 8 != 0)
+        return FA_ERR_INVALID_ARG;
+  } else {
+    return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+int kvcache_splits(const fa_kvcache_args* a, int32_t requested, const DeviceInfo& di) {
+  const int g = a->hq / a->hkv;
+  const int64_t units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
+  const int64_t slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
+  const int64_t nblk = ceil_div64(a->max_seqlen_k, decode_block_n(a->d));
+  int ns = requested > 0 ? requested : fa_num_splits_heuristic(units, slots, nblk, kMaxSplits);
+  const int64_t cap = nblk > 0 ? nblk : 1;
+  if (ns > cap) ns = static_cast<int>(cap);
+  return ns < 1 ? 1 : ns;
+}
+
 int resolve_splits(const fa_fwd_args* a, int32_t requested, const DeviceInfo& di) {
   SplitShape s{};
   split_shape(a, di, &s);
@@ -425,6 +470,71 @@ fa_status fa_fwd_splitkv_noalloc(const fa_fwd_args* a, int32_t num_splits, int32
   void* scratch = nullptr;
   if (!noalloc_scratch(&scratch)) return FA_ERR_CUDA;
   return fa_fwd_splitkv(a, num_splits, scratch, FA_NOALLOC_SCRATCH_BYTES, splits_used, stream);
+}
+
+fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                         int32_t* splits_used, void* stream) {
+  const fa_status v = validate_kvcache(a);
+  if (v != FA_OK) return v;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  const int ns = kvcache_splits(a, num_splits, di);
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
+  const size_t need = align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * a->d * sizeof(float)));
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int bn = decode_block_n(a->d);
+  const bool paged = a->page_size > 0;
+  // 4-D views (d, hkv, rows, outer): paged rows = page_size, outer = pages; packed rows = total_k, outer = 1
+  const int64_t k_st[3] = {paged ? a->k_strides[0] : a->k_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
+                           a->k_strides[1], a->k_strides[2]};
+  const int64_t v_st[3] = {paged ? a->v_strides[0] : a->v_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
+                           a->v_strides[1], a->v_strides[2]};
+  const int rows_dim = paged ? a->page_size : a->num_pages;
+  const int outer_dim = paged ? a->num_pages : 1;
+  if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, rows_dim, outer_dim, k_st, a->d, bn, false) ||
+      !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, rows_dim, outer_dim, v_st, a->d, bn, false))
+    return FA_ERR_INVALID_ARG;
+  p.q = a->q;
+  p.q_stride_b = a->q_strides[0];
+  p.q_stride_h = a->q_strides[1];
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.b = a->b;
+  p.skv = a->max_seqlen_k;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.kv_limit = 0;
+  p.nblk = static_cast<int>(ceil_div64(a->max_seqlen_k, bn));
+  p.num_splits = ns;
+  p.blocks_per_split = 1;  // set per sequence in the kernel
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  p.status = di.status;
+  p.kv_mode = paged ? kKvPaged : kKvPacked;
+  p.block_table = a->block_table;
+  p.bt_stride = a->block_table_stride;
+  p.page_size = a->page_size;
+  p.seqlens = a->seqlens_k;
+  p.cu_seqlens = a->cu_seqlens_k;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_decode(p, a->d, a->dtype, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (splits_used) *splits_used = ns;
+  const int64_t o_st[3] = {a->o_strides[0], static_cast<int64_t>(a->hq) * a->d, a->o_strides[1]};
+  return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, 1, a->d, a->dtype, a->o, o_st, a->lse, stream);
+}
+
+size_t fa_kvcache_workspace_size(const fa_kvcache_args* a, int32_t num_splits) {
+  if (validate_kvcache(a) != FA_OK || num_splits < 0) return 0;
+  DeviceInfo di;
+  if (num_splits == 0 && !device_info(&di)) return 0;
+  const int ns = num_splits > 0 ? num_splits : kvcache_splits(a, 0, di);
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
+  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
 }
 
 fa_status fa_sync_status(void* stream) {

@@ -32,8 +32,14 @@ struct DecCfg {
   static constexpr int STAGES = (D == 256) ? 2 : 4;
   static constexpr int KV_BYTES = kDecBN * D * 2;        // one K or V block
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int THREADS = 32 * (kDecWarps + 1);
+  // two compute warpgroups + one control warpgroup (producer and three idle
+  // warps) so that registers can move to the compute warps: launched at 168 per
+  // thread, control drops to 40 and compute rises to 232 (256 * 232 + 128 * 40
+  // = 384 * 168)
+  static constexpr int THREADS = 32 * (kDecWarps + 4);
   static constexpr int PRODUCER_WARP = kDecWarps;
+  static constexpr int REG_COMPUTE = 232;
+  static constexpr int REG_CONTROL = 40;
 };
 
 template <int D, int G>
@@ -77,7 +83,12 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t idx) {
 enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
+__device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                              float* red, int warp, int lane, int split, int bi, int kvh,
+                                              int h_first, int blk_lo, int nb, int limit);
+
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecCfg<D>;
   using L = DecLane<D, G>;
   extern __shared__ uint8_t smem_raw[];
@@ -92,8 +103,23 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
   const int groups = p.g / G;                    // CTAs per KV head
   const int kvh = blockIdx.y / groups;
   const int h_first = kvh * p.g + (blockIdx.y % groups) * G;  // first query head of this CTA
-  const int blk_lo = split * p.blocks_per_split;
-  const int blk_hi = min(p.nblk, blk_lo + p.blocks_per_split);
+  // Keys of this sequence and where its rows live (contiguous, paged or packed).
+  int limit = p.kv_limit, nblk = p.nblk, bps = p.blocks_per_split, row_base = 0;
+  if (p.kv_mode != kKvDense) {
+    if (p.kv_mode == kKvPaged) {
+      limit = p.seqlens[bi];
+    } else {
+      row_base = p.cu_seqlens[bi];
+      limit = p.cu_seqlens[bi + 1] - row_base;
+    }
+    limit = max(limit, 0);
+    nblk = (limit + kDecBN - 1) / kDecBN;
+    // every sequence is cut into num_splits ranges of its own length (measured
+    // better balanced than ranges of one size set by the longest sequence)
+    bps = max(1, (nblk + p.num_splits - 1) / p.num_splits);
+  }
+  const int blk_lo = split * bps;
+  const int blk_hi = min(nblk, blk_lo + bps);
   const int nb = max(0, blk_hi - blk_lo);
 
   if (threadIdx.x == 0) {
@@ -105,20 +131,41 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
   }
   __syncthreads();
 
-  if (warp == C::PRODUCER_WARP) {
+  if (warp >= C::PRODUCER_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_CONTROL));
+    if (warp > C::PRODUCER_WARP) {  // idle warps of the control warpgroup
+      __syncthreads();
+      return;
+    }
     if (lane == 0 && nb > 0) {
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       const uint64_t pol = l2_policy_evict_first();
       int issued = 0;
+      // paged: the page of the next block is fetched one iteration ahead, so the
+      // table lookup overlaps the wait for a free slot
+      const int* bt_row = p.block_table + static_cast<int64_t>(bi) * p.bt_stride;
+      int page_next = (p.kv_mode == kKvPaged) ? bt_row[(blk_lo * kDecBN) / p.page_size] : 0;
       for (int i = 0; i < nb; ++i) {
         const int slot = i % C::STAGES, use = i / C::STAGES;
+        const int row = (blk_lo + i) * kDecBN;
+        const int page = page_next;
+        if (p.kv_mode == kKvPaged && i + 1 < nb) page_next = bt_row[(row + kDecBN) / p.page_size];
         if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.status, kSiteDecEmpty)) break;
         uint8_t* st = smem + slot * C::STAGE_BYTES;
-        const int row = (blk_lo + i) * kDecBN;
+        // coordinates (row, outer) of this block in the K/V tensor view
+        int c_row = row, c_outer = bi;
+        if (p.kv_mode == kKvPaged) {
+          // a block never straddles a page: the page size is a multiple of the block
+          c_outer = page;
+          c_row = row % p.page_size;
+        } else if (p.kv_mode == kKvPacked) {
+          c_row = row_base + row;
+          c_outer = 0;
+        }
         mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
-        tma_load_4d_hint(st, &p.tm_k, &full[slot], 0, kvh, row, bi, pol);
-        tma_load_4d_hint(st + C::KV_BYTES, &p.tm_v, &full[slot], 0, kvh, row, bi, pol);
+        tma_load_4d_hint(st, &p.tm_k, &full[slot], 0, kvh, c_row, c_outer, pol);
+        tma_load_4d_hint(st + C::KV_BYTES, &p.tm_v, &full[slot], 0, kvh, c_row, c_outer, pol);
         ++issued;
       }
       for (int i = max(0, issued - C::STAGES); i < issued; ++i)
@@ -126,10 +173,20 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
     }
     __syncwarp();
     __syncthreads();
-    return;
+  } else {
+    // ------------------------------ compute warps ------------------------------
+    // (each register budget covers only its own role's code)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_COMPUTE));
+    compute_split<D, G, BF16>(p, smem, full, empty, red, warp, lane, split, bi, kvh, h_first, blk_lo, nb, limit);
   }
+}
 
-  // ------------------------------ compute warps ------------------------------
+template <int D, int G, bool BF16>
+__device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                              float* red, int warp, int lane, int split, int bi, int kvh,
+                                              int h_first, int blk_lo, int nb, int limit) {
+  using C = DecCfg<D>;
+  using L = DecLane<D, G>;
   const int c = lane % L::LPR;      // dim group of this lane
   const int rg = lane / L::LPR;     // row within a pass
   // dims owned: segment s covers [s * D / SEG + 8 c, + 8)
@@ -162,6 +219,24 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
     const uint8_t* ks = smem + slot * C::STAGE_BYTES;
     const uint8_t* vs = ks + C::KV_BYTES;
     const int key0 = (blk_lo + i) * kDecBN + warp * kDecRowsPerWarp;
+    // the last block of a sequence may hold rows past its end (another sequence's
+    // keys, or cache slots never written): their V rows are zeroed below
+    const bool tail_block = (blk_lo + i + 1) * kDecBN > limit;
+    if (tail_block) {
+      // zero this warp's V rows past the end in shared memory (the TMA copy has
+      // landed: the full barrier was waited on), so the loop below stays as is
+      uint8_t* vw = smem + slot * C::STAGE_BYTES + C::KV_BYTES;
+#pragma unroll
+      for (int ps = 0; ps < L::PASSES; ++ps) {
+        const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+        if (key0 + ps * L::RPP + rg >= limit) {
+#pragma unroll
+          for (int sg = 0; sg < L::SEG; ++sg)
+            *reinterpret_cast<uint4*>(vw + kr * (D * 2) + 2 * (sg * (D / L::SEG) + 8 * c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();
+    }
     // scores (log2 domain, scale folded into q) for this lane's row in each pass
     float sc[L::PASSES][G];
 #pragma unroll
@@ -186,7 +261,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] += __shfl_xor_sync(0xffffffffu, sc[ps][h], x);
       const int key = key0 + ps * L::RPP + rg;
-      if (key >= p.kv_limit) {
+      if (key >= limit) {
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] = -INFINITY;
       }
@@ -227,6 +302,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS) fa_decode_kernel(const __g
         const uint4 u = *reinterpret_cast<const uint4*>(vs + kr * (D * 2) + 2 * (s * (D / L::SEG) + 8 * c));
         unpack8<BF16>(u, vf + 8 * s);
       }
+
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float pr = ex2_approx(sc[ps][h] - mn[h]);

@@ -28,6 +28,13 @@ struct PrefillParams {
   int* status;
 };
 
+// Where the decode kernel finds a sequence's keys.
+enum : int {
+  kKvDense = 0,   // K/V [b][skv][hkv][d]; keys j < kv_limit visible
+  kKvPaged = 1,   // K/V cache [num_pages][page_size][hkv][d] addressed through block_table; seqlens[b] keys
+  kKvPacked = 2,  // K/V [total_k][hkv][d]; sequence b owns rows [cu_seqlens[b], cu_seqlens[b + 1])
+};
+
 // Parameters of the CUDA-core split-KV decode kernel (sq == 1).
 struct DecodeParams {
   CUtensorMap tm_k;  // K [b][skv][hkv][d], box {d, 1, BN, 1}, no swizzle
@@ -43,6 +50,12 @@ struct DecodeParams {
   int kv_limit;      // keys j < kv_limit are visible (min(skv, off + 1) when causal)
   float scale_log2;
   int* status;
+  int kv_mode;                  // kKvDense, kKvPaged or kKvPacked
+  const int* block_table;       // paged: [b][bt_stride] page indices
+  int64_t bt_stride;
+  int page_size;                // paged: keys per page, multiple of the 64-key block
+  const int* seqlens;           // paged: [b] keys per sequence
+  const int* cu_seqlens;        // packed: [b + 1] prefix sums of keys per sequence
 };
 
 struct CombineParams {
