@@ -52,7 +52,10 @@ def _load():
         lib.oracle_attention.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                          ctypes.c_double, ip, i64, dp, dp, ctypes.c_int]
         lib.oracle_attention.restype = ctypes.c_int
-        lib.oracle_attention_tiled.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64,
+        lib.oracle_attention_window.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64,
+                                                i64, ctypes.c_double, ip, i64, dp, dp, ctypes.c_int]
+        lib.oracle_attention_window.restype = ctypes.c_int
+        lib.oracle_attention_tiled.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64, i64,
                                                ctypes.c_double, ip, i64, i64, i64, dp, dp, dp, dp,
                                                ctypes.c_int]
         lib.oracle_attention_tiled.restype = ctypes.c_int
@@ -60,6 +63,8 @@ def _load():
         lib.oracle_combine.restype = None
         lib.oracle_visible.argtypes = [i64, i64, i64, ctypes.c_int, i64, ctypes.c_int]
         lib.oracle_visible.restype = ctypes.c_int
+        lib.oracle_visible_window.argtypes = [i64, i64, i64, ctypes.c_int, i64, i64, i64, ctypes.c_int]
+        lib.oracle_visible_window.restype = ctypes.c_int
         lib.oracle_split_efficiency.argtypes = [i64, i64, i64]
         lib.oracle_split_efficiency.restype = ctypes.c_double
         lib.oracle_num_splits.argtypes = [i64, i64, i64, i64]
@@ -99,9 +104,10 @@ def default_offset(sq: int, skv: int) -> int:
 
 
 def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None, scale: float | None = None,
-              rows=None, mutation: int = 0):
+              rows=None, mutation: int = 0, window=(-1, -1)):
     """Direct definition.  Returns (O [nrows, d], LSE [nrows]) for the given rows
-    (default: all rows, ordered batch, head, query)."""
+    (default: all rows, ordered batch, head, query).  window = (left, right) widths of
+    the sliding window around key i + offset; -1 leaves a side unbounded."""
     lib = _load()
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     b, sq, skv, hq, hkv, d = _shapes(q, k, v)
@@ -111,9 +117,10 @@ def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None,
     n = rows.shape[0]
     o = np.zeros((n, d), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    rc = lib.oracle_attention(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off, sc,
-                              rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _dp(o), _dp(lse),
-                              int(mutation))
+    wl, wr = (int(window[0]), int(window[1]))
+    rc = lib.oracle_attention_window(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off, wl, wr, sc,
+                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _dp(o), _dp(lse),
+                                     int(mutation))
     if rc != 0:
         raise ValueError("oracle_attention: bad arguments")
     return o, lse
@@ -121,7 +128,7 @@ def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None,
 
 def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = False,
                     q_pos_offset: int | None = None, scale: float | None = None, rows=None, mutation: int = 0,
-                    return_partials: bool = False):
+                    return_partials: bool = False, window=(-1, -1)):
     """Tile-by-tile online-softmax model (optionally split over the key axis and merged)."""
     lib = _load()
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -134,7 +141,8 @@ def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = F
     lse = np.zeros((n,), dtype=np.float64)
     op = np.zeros((num_splits, n, d), dtype=np.float64)
     lp = np.zeros((num_splits, n), dtype=np.float64)
-    rc = lib.oracle_attention_tiled(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off, sc,
+    rc = lib.oracle_attention_tiled(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off,
+                                    int(window[0]), int(window[1]), sc,
                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, int(tile),
                                     int(num_splits), _dp(o), _dp(lse), _dp(op), _dp(lp), int(mutation))
     if rc != 0:
@@ -158,8 +166,9 @@ def combine(o_part, lse_part):
     return o, lse
 
 
-def visible(i: int, j: int, skv: int, causal: bool, q_pos_offset: int, mutation: int = 0) -> bool:
-    return bool(_load().oracle_visible(i, j, skv, int(causal), int(q_pos_offset), int(mutation)))
+def visible(i: int, j: int, skv: int, causal: bool, q_pos_offset: int, mutation: int = 0, window=(-1, -1)) -> bool:
+    return bool(_load().oracle_visible_window(i, j, skv, int(causal), int(q_pos_offset), int(window[0]),
+                                              int(window[1]), int(mutation)))
 
 
 def split_efficiency(units: int, slots: int, s: int) -> float:

@@ -31,8 +31,14 @@
  *   oracle_num_splits       section 7.2 of the same page: the smallest split
  *                           count whose occupancy is at least 85% of the best.
  *
+ * Sliding-window (local) attention follows "flash attention V2 code walkthrough",
+ * template flag Is_local: query i sees keys in [i + skv - sq - window_left,
+ * i + skv - sq + window_right], written here with the general query offset off
+ * in place of skv - sq; a negative window width leaves that side unbounded.
+ *
  * Conventions for what the pages leave open (each is listed in the design notes):
- *   - a query row i sees key j iff j < skv and (not causal or j <= i + off);
+ *   - a query row i sees key j iff j < skv and (not causal or j <= i + off)
+ *     and, with a window, i + off - window_left <= j <= i + off + window_right;
  *   - a row that sees no key gets O = 0 and LSE = -inf;
  *   - the scale multiplies the raw dot product before mask and max; LSE is in
  *     natural-log units of the scaled scores;
@@ -52,14 +58,21 @@
 #define ORACLE_MUT_STRICT_CAUSAL 4   /* both: causal j <= i + off replaced by j < ... */
 #define ORACLE_MUT_NO_ALPHA_ON_L 8   /* tiled: old denominator not rescaled by alpha */
 
-int oracle_version(void) { return 1; }
+int oracle_version(void) { return 2; }
 
-/* Visibility of key j to query row i. */
-int oracle_visible(int64_t i, int64_t j, int64_t skv, int causal, int64_t off, int mutation) {
+/* Visibility of key j to query row i; wl / wr < 0: that side of the window is unbounded. */
+int oracle_visible_window(int64_t i, int64_t j, int64_t skv, int causal, int64_t off, int64_t wl, int64_t wr,
+                          int mutation) {
   if (j < 0 || j >= skv) return 0;
+  if (wl >= 0 && j < i + off - wl) return 0;
+  if (wr >= 0 && j > i + off + wr) return 0;
   if (!causal) return 1;
   if (mutation & ORACLE_MUT_STRICT_CAUSAL) return j < i + off;
   return j <= i + off;
+}
+
+int oracle_visible(int64_t i, int64_t j, int64_t skv, int causal, int64_t off, int mutation) {
+  return oracle_visible_window(i, j, skv, causal, off, -1, -1, mutation);
 }
 
 static double dot(const double* a, const double* b, int64_t d) {
@@ -75,9 +88,9 @@ static double dot(const double* a, const double* b, int64_t d) {
  *   o: [nrows][d], lse: [nrows].
  * Returns 0 on success, -1 on bad arguments.
  */
-int oracle_attention(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
-                     int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, double scale,
-                     const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
+int oracle_attention_window(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
+                            int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
+                            double scale, const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0) return -1;
   const int64_t g = hq / hkv;
   const double sc = (mutation & ORACLE_MUT_NO_SCALE) ? 1.0 : scale;
@@ -104,7 +117,7 @@ int oracle_attention(const double* q, const double* k, const double* v, int64_t 
       double m = -INFINITY;
       int64_t nvis = 0;
       for (int64_t j = 0; j < skv; ++j) {
-        if (!oracle_visible(i, j, skv, causal, off, mutation)) continue;
+        if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, mutation)) continue;
         s[j] = sc * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
         if (s[j] > m) m = s[j];
         ++nvis;
@@ -116,7 +129,7 @@ int oracle_attention(const double* q, const double* k, const double* v, int64_t 
       }
       double l = 0.0;
       for (int64_t j = 0; j < skv; ++j) {
-        if (!oracle_visible(i, j, skv, causal, off, mutation)) continue;
+        if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, mutation)) continue;
         const double p = exp(s[j] - m);
         const double* vrow = v + ((bi * skv + j) * hkv + kvh) * d;
         l += p;
@@ -128,6 +141,13 @@ int oracle_attention(const double* q, const double* k, const double* v, int64_t 
     free(s);
   }
   return bad ? -1 : 0;
+}
+
+int oracle_attention(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
+                     int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, double scale,
+                     const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
+  return oracle_attention_window(q, k, v, b, sq, skv, hq, hkv, d, causal, off, -1, -1, scale, rows, nrows, o, lse,
+                                 mutation);
 }
 
 /*
@@ -166,7 +186,8 @@ void oracle_combine(const double* o_part, const double* lse_part, int64_t ns, in
  * output and the LSE of this range (0 / -inf when nothing in it is visible).
  */
 static void one_row_tiled(const double* qrow, const double* k, const double* v, int64_t bi, int64_t i,
-                          int64_t skv, int64_t hkv, int64_t kvh, int64_t d, int causal, int64_t off, double sc,
+                          int64_t skv, int64_t hkv, int64_t kvh, int64_t d, int causal, int64_t off, int64_t wl,
+                          int64_t wr, double sc,
                           int64_t tile, int64_t t_lo, int64_t t_hi, int mutation, double* s, double* p, double* o,
                           double* lse) {
   double m = -INFINITY, l = 0.0;
@@ -177,7 +198,7 @@ static void one_row_tiled(const double* qrow, const double* k, const double* v, 
     int any = 0;
     double bmax = -INFINITY;
     for (int64_t j = j0; j < j1; ++j) {
-      if (oracle_visible(i, j, skv, causal, off, mutation)) {
+      if (oracle_visible_window(i, j, skv, causal, off, wl, wr, mutation)) {
         s[j - j0] = sc * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
         if (s[j - j0] > bmax) bmax = s[j - j0];
         any = 1;
@@ -221,9 +242,9 @@ static void one_row_tiled(const double* qrow, const double* k, const double* v, 
  * per-split partials, [num_splits][nrows][d] and [num_splits][nrows].
  */
 int oracle_attention_tiled(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
-                           int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, double scale,
-                           const int64_t* rows, int64_t nrows, int64_t tile, int64_t num_splits, double* o,
-                           double* lse, double* o_part, double* lse_part, int mutation) {
+                           int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
+                           double scale, const int64_t* rows, int64_t nrows, int64_t tile, int64_t num_splits,
+                           double* o, double* lse, double* o_part, double* lse_part, int mutation) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || tile <= 0 || num_splits <= 0) return -1;
   const int64_t g = hq / hkv;
   const double sc = (mutation & ORACLE_MUT_NO_SCALE) ? 1.0 : scale;
@@ -258,7 +279,8 @@ int oracle_attention_tiled(const double* q, const double* k, const double* v, in
         int64_t t_lo = sp * nbps, t_hi = (sp + 1) * nbps;
         if (t_hi > nblk) t_hi = nblk;
         if (t_lo > t_hi) t_lo = t_hi;
-        one_row_tiled(qrow, k, v, bi, i, skv, hkv, hi / g, d, causal, off, sc, tile, t_lo, t_hi, mutation, s, p,
+        one_row_tiled(qrow, k, v, bi, i, skv, hkv, hi / g, d, causal, off, wl, wr, sc, tile, t_lo, t_hi, mutation, s,
+                      p,
                       o_part + (sp * nrows + r) * d, lse_part + sp * nrows + r);
       }
     }

@@ -290,6 +290,71 @@ def test_split_heuristic_bounds(oracle_mod):
         assert all(oracle_mod.split_efficiency(units, 152, t) < 0.85 * best for t in range(1, s))
 
 
+# ---------------------------------------------------------------- sliding window
+
+
+def _band_reference(q, k, v, off, wl, wr, scale, causal=False):
+    """torch's fp64 CPU attention with a band mask from tril/triu of a ones matrix (library routines)."""
+    sq, skv = q.shape[1], k.shape[1]
+    band = torch.ones(sq, skv, dtype=torch.bool)
+    if wr >= 0:
+        band = band.tril(off + wr)
+    if wl >= 0:
+        band = band.triu(off - wl)
+    if causal:
+        band = band & torch.ones(sq, skv, dtype=torch.bool).tril(off)
+    add = torch.zeros(sq, skv, dtype=torch.float64).masked_fill(~band, float("-inf"))
+    qt = torch.from_numpy(q).permute(0, 2, 1, 3).contiguous()
+    kt = torch.from_numpy(k).permute(0, 2, 1, 3).contiguous()
+    vt = torch.from_numpy(v).permute(0, 2, 1, 3).contiguous()
+    g = qt.shape[1] // kt.shape[1]
+    kt, vt = kt.repeat_interleave(g, dim=1), vt.repeat_interleave(g, dim=1)
+    out, lse = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(qt, kt, vt, 0.0, False, attn_mask=add,
+                                                                           scale=scale)[:2]
+    return out.permute(0, 2, 1, 3).numpy(), lse.numpy(), band.numpy()
+
+
+WINDOW_CASES = [
+    # b, sq, skv, hq, hkv, d, off, wl, wr, causal
+    (1, 9, 9, 2, 1, 8, 0, 3, 0, False),
+    (2, 7, 12, 2, 2, 16, 5, 2, 4, False),
+    (1, 10, 10, 4, 2, 8, 0, 4, -1, True),
+    (1, 6, 20, 2, 2, 8, 14, -1, 3, False),
+    (1, 11, 11, 2, 1, 8, 0, 0, 0, False),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES)
+def test_window_matches_library_band_mask(oracle_mod, case):
+    b, sq, skv, hq, hkv, d, off, wl, wr, causal = case
+    rng = np.random.default_rng(sum(case[:6]) + 17)
+    q, k, v = _qkv(rng, b, sq, skv, hq, hkv, d, std=1.3)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle_mod.attention(q, k, v, causal=causal, q_pos_offset=off, window=(wl, wr))
+    ro, rl, band = _band_reference(q, k, v, off, wl, wr, scale, causal)
+    rows = oracle_mod.all_rows(b, hq, sq)
+    np.testing.assert_allclose(o, ro[rows[:, 0], rows[:, 2], rows[:, 1]], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, rl[rows[:, 0], rows[:, 1], rows[:, 2]], rtol=0, atol=1e-12)
+    for i in range(sq):
+        for j in range(skv):
+            assert oracle_mod.visible(i, j, skv, causal, off, window=(wl, wr)) == bool(band[i, j])
+    for tile in (1, 3, 4):
+        ot, lt = oracle_mod.attention_tiled(q, k, v, tile=tile, num_splits=2, causal=causal, q_pos_offset=off,
+                                            window=(wl, wr))
+        np.testing.assert_allclose(ot, o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lt, lse, rtol=0, atol=1e-12)
+
+
+def test_window_right_zero_is_causal(oracle_mod):
+    """The page's causal flag is the window (unbounded, 0): same visibility everywhere."""
+    for (sq, skv) in ((2, 5), (5, 2), (7, 7)):
+        off = skv - sq
+        for i in range(sq):
+            for j in range(skv):
+                assert oracle_mod.visible(i, j, skv, True, off) == oracle_mod.visible(i, j, skv, False, off,
+                                                                                      window=(-1, 0))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 
