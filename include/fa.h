@@ -7,7 +7,9 @@
  *   for every batch b, query head h, query row i:
  *     kv_head  = h / (hq / hkv)                      (GQA mapping, "flash attention V2
  *                                                     code walkthrough", block_table / h_h_k_ratio)
- *     visible  = { j < skv : !causal || j <= i + q_pos_offset }
+ *     visible  = { j < skv : (!causal || j <= i + q_pos_offset)
+ *                  && (!local || window_left < 0  || j >= i + q_pos_offset - window_left)
+ *                  && (!local || window_right < 0 || j <= i + q_pos_offset + window_right) }
  *     s_j      = scale * <Q[b,i,h,:], K[b,j,kv_head,:]>
  *     O[b,i,h] = sum_j softmax(s)_j V[b,j,kv_head,:]   over visible j
  *     LSE[b,h,i] = log sum_j exp(s_j)                  over visible j
@@ -16,7 +18,11 @@
  * The causal rule is bottom-right aligned by default (q_pos_offset = skv - sq,
  * the mask pictures of "flash attention V2 code walkthrough", Is_causal); any
  * other offset gives the absolute query position used by a KV-cache decode
- * ("hs-black", section "Implementation: causal and tail blocks").
+ * ("hs-black", section "Implementation: causal and tail blocks").  The sliding
+ * window ("flash attention V2 code walkthrough", Is_local: query i attends to
+ * keys [i + skv - sq - window_left, i + skv - sq + window_right], -1 leaving a
+ * side open) is aligned on the same diagonal; causal is the window (-1, 0), and
+ * causal together with a window keeps the keys both allow.
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
@@ -78,16 +84,21 @@ typedef struct {
   int64_t o_strides[3];
   int32_t causal;       /* 0 or 1 */
   int64_t q_pos_offset; /* causal: row i sees key j iff j <= i + q_pos_offset;
-                           FA_OFFSET_BOTTOM_RIGHT = skv - sq.  Ignored when causal == 0. */
+                           FA_OFFSET_BOTTOM_RIGHT = skv - sq.  Ignored when causal == 0 and local == 0. */
   float scale;          /* multiplies q.k before the mask and the max; finite, > 0 (e.g. 1/sqrt(d)) */
+  int32_t local;        /* 0 or 1: apply the sliding window below (ABI version >= 2) */
+  int64_t window_left;  /* local: row i sees keys j >= i + q_pos_offset - window_left; -1 = no left edge */
+  int64_t window_right; /* local: row i sees keys j <= i + q_pos_offset + window_right; -1 = no right edge */
 } fa_fwd_args;
 
 /*
  * Prefill / general forward pass: O and LSE for every row.
  * Tiled exactly as "ai-reference-codex: forward CUDA kernel", sections 2-6: a
  * CTA owns Q row blocks, K/V blocks stream past, blocks beyond the causal
- * diagonal are skipped, the elementwise mask runs only on diagonal and tail
- * blocks, and the epilogue divides by l and writes LSE = m + log l.
+ * diagonal (or outside the sliding window: n_block_min / n_block_max of "flash
+ * attention V2 code walkthrough", section 2) are skipped, the elementwise mask
+ * runs only on the blocks an edge cuts, and the epilogue divides by l and
+ * writes LSE = m + log l.
  * Returns FA_OK once the work is enqueued on `stream`.
  */
 fa_status fa_fwd(const fa_fwd_args* args, void* stream);
@@ -165,8 +176,10 @@ fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t
  *   packed  (page_size == 0): k, v are [total_k, hkv, d] with sequence b at rows
  *           [cu_seqlens_k[b], cu_seqlens_k[b + 1]); num_pages holds total_k.
  * The query of sequence b sees every one of its keys (it stands at position
- * len_b - 1); a sequence with no key gets O = 0, LSE = -inf.  Rows of the
- * cache beyond a sequence's length are never used, whatever they hold.
+ * len_b - 1), or with local = 1 only the last window_left + 1 of them (the
+ * sliding window of fa_fwd_args, right edge at the query itself); a sequence
+ * with no key gets O = 0, LSE = -inf.  Rows of the cache beyond a sequence's
+ * length, or before its window, are never used, whatever they hold.
  */
 typedef struct {
   fa_dtype dtype;
@@ -188,6 +201,8 @@ typedef struct {
   int64_t o_strides[2];           /* (batch, head), in elements */
   float* lse;                     /* device, fp32 [b, hq] */
   float scale;
+  int32_t local;                  /* 0 or 1 (ABI version >= 2) */
+  int32_t window_left;            /* local: keys at positions >= len_b - 1 - window_left; -1 = all */
 } fa_kvcache_args;
 
 /* Workspace bytes fa_fwd_kvcache needs for num_splits splits (0 = its default); 0 if invalid. */

@@ -4,6 +4,8 @@ device, and its split heuristic agrees with the oracle's."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -37,7 +39,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_version() == 1
+    assert lib.fa_version() == 2
     for code in range(5):
         assert lib.fa_status_string(code)
     assert lib.fa_status_string(99) == b"unknown status"
@@ -72,11 +74,70 @@ def _args(**kw):
 @pytest.mark.parametrize("field,value,expect", [
     ("dtype", 7, 1), ("b", 0, 1), ("hq", 3, 1), ("causal", 2, 1), ("scale", 0.0, 1),
     ("scale", float("nan"), 1), ("d", 96, 2), ("d", 32, 2), ("q", 0, 1), ("lse", 0, 1), ("q", 4100, 1),
+    ("local", 2, 1),
 ])
 def test_validation_rejects_before_any_launch(lib, field, value, expect):
     a = _args(**{field: value})
     assert lib.fa_fwd(ctypes.byref(a), None) == expect
     assert lib.fa_fwd_splitkv(ctypes.byref(a), 1, None, 0, None, None) == expect
+
+
+def test_window_widths_below_minus_one_rejected(lib):
+    for wl, wr in ((-2, 0), (0, -2), (-5, -5)):
+        a = _args(local=1, window_left=wl, window_right=wr)
+        assert lib.fa_fwd(ctypes.byref(a), None) == 1
+        assert lib.fa_fwd_splitkv(ctypes.byref(a), 1, None, 0, None, None) == 1
+    # the widths are not looked at while local == 0
+    a = _args(local=0, window_left=-7, window_right=-7, q=4100)
+    assert lib.fa_fwd(ctypes.byref(a), None) == 1  # rejected for the misaligned q only
+    a = _kv_args(local=1, window_left=-2)
+    assert lib.fa_fwd_kvcache(ctypes.byref(a), 0, None, 0, None, None) == 1
+    a = _kv_args(local=3)
+    assert lib.fa_fwd_kvcache(ctypes.byref(a), 0, None, 0, None, None) == 1
+
+
+_LAYOUT_PROBE = r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "fa.h"
+#define F(T, f) printf(#T " " #f " %zu %zu\n", offsetof(T, f), sizeof(((T*)0)->f));
+int main(void) {
+  printf("fa_fwd_args size %zu\n", sizeof(fa_fwd_args));
+  printf("fa_kvcache_args size %zu\n", sizeof(fa_kvcache_args));
+  FIELDS
+  return 0;
+}
+'''
+
+
+def test_ctypes_mirrors_match_header_layout(tmp_path):
+    """Every field of the ctypes mirrors sits at the offset, with the size, that a C
+    compiler gives the structs declared in include/fa.h."""
+    from tiled_exact_attention_gb300._lib import FwdArgs, KvcacheArgs
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    fields = []
+    for cname, py in (("fa_fwd_args", FwdArgs), ("fa_kvcache_args", KvcacheArgs)):
+        for name, _ in py._fields_:
+            fields.append(f"F({cname}, {name})")
+    src = tmp_path / "layout.c"
+    src.write_text(_LAYOUT_PROBE.replace("FIELDS", "\n  ".join(fields)))
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
+    sizes = {ln.split()[0]: int(ln.split()[2]) for ln in out if ln.split()[1] == "size"}
+    assert sizes["fa_fwd_args"] == ctypes.sizeof(FwdArgs)
+    assert sizes["fa_kvcache_args"] == ctypes.sizeof(KvcacheArgs)
+    for ln in out:
+        parts = ln.split()
+        if parts[1] == "size":
+            continue
+        struct, name, off, size = parts[0], parts[1], int(parts[2]), int(parts[3])
+        py = FwdArgs if struct == "fa_fwd_args" else KvcacheArgs
+        desc = getattr(py, name)
+        assert (desc.offset, desc.size) == (off, size), (struct, name)
 
 
 def test_validation_strides_and_null(lib):

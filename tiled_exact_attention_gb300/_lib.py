@@ -62,6 +62,9 @@ class FwdArgs(ctypes.Structure):
         ("causal", ctypes.c_int32),
         ("q_pos_offset", ctypes.c_int64),
         ("scale", ctypes.c_float),
+        ("local", ctypes.c_int32),
+        ("window_left", ctypes.c_int64),
+        ("window_right", ctypes.c_int64),
     ]
 
 
@@ -91,6 +94,8 @@ class KvcacheArgs(ctypes.Structure):
         ("o_strides", ctypes.c_int64 * 2),
         ("lse", ctypes.c_void_p),
         ("scale", ctypes.c_float),
+        ("local", ctypes.c_int32),
+        ("window_left", ctypes.c_int32),
     ]
 
 

@@ -45,7 +45,9 @@ def _check_qkv(q, k, v):
         raise ValueError("inconsistent q/k/v shapes")
 
 
-def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offset: int | None) -> FwdArgs:
+def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offset: int | None,
+              window=None) -> FwdArgs:
+    """Fill `fa_fwd_args`.  window = (left, right) turns on the sliding window (-1 leaves a side open)."""
     _check_qkv(q, k, v)
     b, sq, hq, d = q.shape
     skv, hkv = k.shape[1], k.shape[2]
@@ -58,6 +60,9 @@ def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offse
     a.causal = 1 if causal else 0
     a.q_pos_offset = FA_OFFSET_BOTTOM_RIGHT if q_pos_offset is None else int(q_pos_offset)
     a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    if window is not None:
+        a.local = 1
+        a.window_left, a.window_right = int(window[0]), int(window[1])
     return a
 
 
@@ -75,10 +80,10 @@ def _outputs(q, out, lse):
 
 
 def fa_fwd(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
-           out=None, lse=None, stream=None):
+           out=None, lse=None, stream=None, window=None):
     """Forward pass; returns (O, LSE)."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
     check(_lib.load().fa_fwd(ctypes.byref(a), _stream_handle(stream)), "fa_fwd")
     return out, lse
 
@@ -87,24 +92,25 @@ def fa_num_splits_heuristic(units: int, slots: int, num_kv_blocks: int, max_spli
     return int(_lib.load().fa_num_splits_heuristic(units, slots, num_kv_blocks, max_splits))
 
 
-def fa_splitkv_default_splits(q, k, v, *, causal=False, scale=None, q_pos_offset=None) -> int:
+def fa_splitkv_default_splits(q, k, v, *, causal=False, scale=None, q_pos_offset=None, window=None) -> int:
     out, lse = _outputs(q, None, None)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
     return int(_lib.load().fa_splitkv_default_splits(ctypes.byref(a)))
 
 
 def fa_splitkv_workspace_size(q, k, v, num_splits: int = 0, *, causal=False, scale=None,
-                              q_pos_offset=None) -> int:
+                              q_pos_offset=None, window=None) -> int:
     out, lse = _outputs(q, None, None)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
     return int(_lib.load().fa_splitkv_workspace_size(ctypes.byref(a), num_splits))
 
 
 def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
-                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None, return_splits=False):
+                   num_splits: int = 0, workspace=None, out=None, lse=None, stream=None, return_splits=False,
+                   window=None):
     """Split-KV forward + combine; returns (O, LSE) (and the split count if asked)."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
     lib = _lib.load()
     need = int(lib.fa_splitkv_workspace_size(ctypes.byref(a), int(num_splits)))
     if workspace is None:
@@ -120,10 +126,10 @@ def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None,
 
 def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None = None,
                            q_pos_offset: int | None = None, num_splits: int = 0, out=None, lse=None, stream=None,
-                           return_splits=False):
+                           return_splits=False, window=None):
     """Split-KV forward that uses the library's built-in scratch instead of a workspace."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
     used = ctypes.c_int32(0)
     check(_lib.load().fa_fwd_splitkv_noalloc(ctypes.byref(a), int(num_splits), ctypes.byref(used),
                                              _stream_handle(stream)), "fa_fwd_splitkv_noalloc")
@@ -133,9 +139,10 @@ def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None
 
 
 def make_kvcache_args(q, k, v, o, lse, *, block_table=None, seqlens_k=None, cu_seqlens_k=None,
-                      max_seqlen_k: int = 0, scale: float | None = None) -> KvcacheArgs:
+                      max_seqlen_k: int = 0, scale: float | None = None, window_left=None) -> KvcacheArgs:
     """Fill `fa_kvcache_args`.  q, o: [b, hq, d]; paged k/v: [num_pages, page_size, hkv, d] with
-    block_table [b, n] and seqlens_k [b] (int32); packed k/v: [total_k, hkv, d] with cu_seqlens_k [b + 1]."""
+    block_table [b, n] and seqlens_k [b] (int32); packed k/v: [total_k, hkv, d] with cu_seqlens_k [b + 1].
+    window_left (not None) keeps only the last window_left + 1 keys of each sequence."""
     for name, t in (("q", q), ("k", k), ("v", v), ("out", o)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in _DT or t.stride(-1) != 1:
             raise ValueError(f"{name} must be a CUDA bf16/fp16 tensor with a contiguous last dimension")
@@ -174,12 +181,14 @@ def make_kvcache_args(q, k, v, o, lse, *, block_table=None, seqlens_k=None, cu_s
     a.o_strides = (ctypes.c_int64 * 2)(o.stride(0), o.stride(1))
     a.lse = lse.data_ptr()
     a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    if window_left is not None:
+        a.local, a.window_left = 1, int(window_left)
     return a
 
 
 def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=None, max_seqlen_k=None,
                    scale=None, num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
-                   return_splits=False):
+                   return_splits=False, window_left=None):
     """Decode one query row per sequence against a paged or packed KV cache; returns (O [b, hq, d], LSE [b, hq])."""
     if out is None:
         out = torch.empty_like(q)
@@ -189,7 +198,8 @@ def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=No
         lens = seqlens_k if block_table is not None else (cu_seqlens_k[1:] - cu_seqlens_k[:-1])
         max_seqlen_k = int(lens.max().item()) if lens.numel() else 0
     a = make_kvcache_args(q, k, v, out, lse, block_table=block_table, seqlens_k=seqlens_k,
-                          cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, scale=scale)
+                          cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, scale=scale,
+                          window_left=window_left)
     lib = _lib.load()
     if workspace is None:
         need = int(lib.fa_kvcache_workspace_size(ctypes.byref(a), int(num_splits)))

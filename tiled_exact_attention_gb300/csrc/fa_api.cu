@@ -85,6 +85,8 @@ fa_status validate(const fa_fwd_args* a) {
   if (a->b < 1 || a->sq < 0 || a->skv < 0 || a->hq < 1 || a->hkv < 1) return FA_ERR_INVALID_ARG;
   if (a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
   if (a->causal != 0 && a->causal != 1) return FA_ERR_INVALID_ARG;
+  if (a->local != 0 && a->local != 1) return FA_ERR_INVALID_ARG;
+  if (a->local && (a->window_left < -1 || a->window_right < -1)) return FA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
   if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->sq > (1 << 30) || a->skv > (1 << 30)) return FA_ERR_UNSUPPORTED;
@@ -120,32 +122,62 @@ bool encode_map(CUtensorMap* m, const void* ptr, fa_dtype dt, int d, int h, int 
 
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Causal offset as the kernels use it: j <= i + off.  Returns false when the
-// causal constraint hides nothing (then the problem is treated as non-causal).
-struct CausalPlan {
+// The mask as the kernels use it: row i sees key j < skv only if
+// j <= i + off (when causal) and j >= i + left_off (when local).  An edge that
+// hides nothing is dropped; offsets are clamped to where every row sees nothing,
+// so they fit in an int.
+struct MaskPlan {
   int causal;
   int off;
+  int local;
+  int left_off;
 };
 
-CausalPlan plan_causal(const fa_fwd_args* a) {
-  CausalPlan c{0, 0};
-  if (!a->causal) return c;
-  int64_t off = a->q_pos_offset == FA_OFFSET_BOTTOM_RIGHT ? static_cast<int64_t>(a->skv) - a->sq : a->q_pos_offset;
-  if (off >= static_cast<int64_t>(a->skv) - 1) return c;  // row 0 already sees every key
-  if (off < -static_cast<int64_t>(a->sq) - 1) off = -static_cast<int64_t>(a->sq) - 1;  // every row sees nothing
-  c.causal = 1;
-  c.off = static_cast<int>(off);
+MaskPlan plan_mask(const fa_fwd_args* a) {
+  MaskPlan c{0, 0, 0, 0};
+  constexpr int64_t kBig = static_cast<int64_t>(1) << 40;  // beyond any row or key index
+  const int64_t sq = a->sq, skv = a->skv;
+  int64_t base = a->q_pos_offset == FA_OFFSET_BOTTOM_RIGHT ? skv - sq : a->q_pos_offset;
+  base = base < -kBig ? -kBig : (base > kBig ? kBig : base);
+  const bool right_win = a->local && a->window_right >= 0;
+  if (a->causal || right_win) {
+    int64_t off = kBig;
+    if (a->causal) off = base;
+    if (right_win) {
+      const int64_t w = a->window_right > kBig ? kBig : a->window_right;
+      off = off < base + w ? off : base + w;
+    }
+    if (off < skv - 1) {  // otherwise row 0 already sees every key
+      c.causal = 1;
+      c.off = static_cast<int>(off < -sq - 1 ? -sq - 1 : off);  // below: every row sees nothing
+    }
+  }
+  if (a->local && a->window_left >= 0) {
+    const int64_t w = a->window_left > kBig ? kBig : a->window_left;
+    const int64_t lo = base - w;
+    if (lo + sq - 1 > 0) {  // otherwise even the last row's edge is at or before key 0
+      c.local = 1;
+      c.left_off = static_cast<int>(lo > skv ? skv : lo);  // above: every row sees nothing
+    }
+  }
   return c;
 }
 
 bool use_decode_kernel(const fa_fwd_args* a) { return a->sq == 1 && decode_supported(a->d, a->hq / a->hkv); }
 
-// Keys a decode row can see (sq == 1): j < kv_limit.
+// Keys a decode row can see (sq == 1): kv_start <= j < kv_limit.
 int decode_kv_limit(const fa_fwd_args* a) {
-  const CausalPlan c = plan_causal(a);
+  const MaskPlan c = plan_mask(a);
   if (!c.causal) return a->skv;
   const int64_t lim = static_cast<int64_t>(c.off) + 1;
   return static_cast<int>(lim < 0 ? 0 : (lim > a->skv ? a->skv : lim));
+}
+
+int decode_kv_start(const fa_fwd_args* a) {
+  const MaskPlan c = plan_mask(a);
+  if (!c.local) return 0;
+  const int lim = decode_kv_limit(a);
+  return c.left_off < 0 ? 0 : (c.left_off > lim ? lim : c.left_off);
 }
 
 struct SplitShape {
@@ -159,7 +191,7 @@ bool split_shape(const fa_fwd_args* a, const DeviceInfo& di, SplitShape* s) {
     const int g = a->hq / a->hkv;
     s->units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
     s->slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
-    s->nblk = ceil_div64(decode_kv_limit(a), decode_block_n(a->d));
+    s->nblk = ceil_div64(decode_kv_limit(a), decode_block_n(a->d)) - decode_kv_start(a) / decode_block_n(a->d);
   } else {
     const int nq = prefill_q_tiles(a->d);
     const int64_t n_mcta = ceil_div64(ceil_div64(a->sq, 128), nq);
@@ -207,6 +239,7 @@ fa_status validate_kvcache(const fa_kvcache_args* a) {
   if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
   if (a->b < 1 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if ((a->local != 0 && a->local != 1) || (a->local && a->window_left < -1)) return FA_ERR_INVALID_ARG;
   if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->max_seqlen_k < 0 || a->max_seqlen_k > (1 << 30) || a->num_pages < 1) return FA_ERR_INVALID_ARG;
   if (a->q == nullptr || a->k == nullptr || a->v == nullptr || a->o == nullptr || a->lse == nullptr)
@@ -234,7 +267,9 @@ int kvcache_splits(const fa_kvcache_args* a, int32_t requested, const DeviceInfo
   const int g = a->hq / a->hkv;
   const int64_t units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
   const int64_t slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
-  const int64_t nblk = ceil_div64(a->max_seqlen_k, decode_block_n(a->d));
+  int64_t keys = a->max_seqlen_k;
+  if (a->local && a->window_left >= 0 && a->window_left + 1 < keys) keys = a->window_left + 1 + decode_block_n(a->d);
+  const int64_t nblk = ceil_div64(keys, decode_block_n(a->d));
   int ns = requested > 0 ? requested : fa_num_splits_heuristic(units, slots, nblk, kMaxSplits);
   const int64_t cap = nblk > 0 ? nblk : 1;
   if (ns > cap) ns = static_cast<int>(cap);
@@ -259,7 +294,7 @@ using namespace fa;
 
 extern "C" {
 
-int32_t fa_version(void) { return 1; }
+int32_t fa_version(void) { return 2; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -303,7 +338,7 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
       (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
        !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, bn, true)))
     return FA_ERR_INVALID_ARG;
-  const CausalPlan c = plan_causal(a);
+  const MaskPlan c = plan_mask(a);
   p.o = a->o;
   p.lse = a->lse;
   p.o_part = nullptr;
@@ -318,6 +353,8 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   p.g = a->hq / a->hkv;
   p.causal = c.causal;
   p.off = c.off;
+  p.local = c.local;
+  p.left_off = c.left_off;
   p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
   p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
   p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
@@ -412,9 +449,12 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     p.hkv = a->hkv;
     p.g = a->hq / a->hkv;
     p.kv_limit = decode_kv_limit(a);
+    p.kv_start = decode_kv_start(a);
+    p.window_left = -1;
     p.nblk = static_cast<int>(ceil_div64(p.kv_limit, bn));
     p.num_splits = ns;
-    p.blocks_per_split = static_cast<int>(ceil_div64(p.nblk > 0 ? p.nblk : 1, ns));
+    const int span = p.nblk - p.kv_start / bn;
+    p.blocks_per_split = static_cast<int>(ceil_div64(span > 0 ? span : 1, ns));
     p.scale_log2 = scale_log2;
     p.status = di.status;
     e = launch_decode(p, a->d, a->dtype, st);
@@ -428,7 +468,7 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
         (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
          !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, bn, true)))
       return FA_ERR_INVALID_ARG;
-    const CausalPlan c = plan_causal(a);
+    const MaskPlan c = plan_mask(a);
     p.o = nullptr;
     p.lse = lse_part;
     p.o_part = o_part;
@@ -440,6 +480,8 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     p.g = a->hq / a->hkv;
     p.causal = c.causal;
     p.off = c.off;
+    p.local = c.local;
+    p.left_off = c.left_off;
     p.scale_log2 = scale_log2;
     p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
     p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
@@ -510,6 +552,8 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
   p.hkv = a->hkv;
   p.g = a->hq / a->hkv;
   p.kv_limit = 0;
+  p.kv_start = 0;
+  p.window_left = a->local ? a->window_left : -1;
   p.nblk = static_cast<int>(ceil_div64(a->max_seqlen_k, bn));
   p.num_splits = ns;
   p.blocks_per_split = 1;  // set per sequence in the kernel

@@ -85,7 +85,7 @@ enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int warp, int lane, int split, int bi, int kvh,
-                                              int h_first, int blk_lo, int nb, int limit);
+                                              int h_first, int blk_lo, int nb, int start, int limit);
 
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -103,8 +103,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
   const int groups = p.g / G;                    // CTAs per KV head
   const int kvh = blockIdx.y / groups;
   const int h_first = kvh * p.g + (blockIdx.y % groups) * G;  // first query head of this CTA
-  // Keys of this sequence and where its rows live (contiguous, paged or packed).
-  int limit = p.kv_limit, nblk = p.nblk, bps = p.blocks_per_split, row_base = 0;
+  // Keys of this sequence (start <= j < limit) and where its rows live
+  // (contiguous, paged or packed).
+  int limit = p.kv_limit, start = p.kv_start, nblk = p.nblk, bps = p.blocks_per_split, row_base = 0;
   if (p.kv_mode != kKvDense) {
     if (p.kv_mode == kKvPaged) {
       limit = p.seqlens[bi];
@@ -113,12 +114,14 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
       limit = p.cu_seqlens[bi + 1] - row_base;
     }
     limit = max(limit, 0);
+    start = p.window_left >= 0 ? max(0, limit - 1 - p.window_left) : 0;
     nblk = (limit + kDecBN - 1) / kDecBN;
     // every sequence is cut into num_splits ranges of its own length (measured
     // better balanced than ranges of one size set by the longest sequence)
-    bps = max(1, (nblk + p.num_splits - 1) / p.num_splits);
+    bps = max(1, (nblk - start / kDecBN + p.num_splits - 1) / p.num_splits);
   }
-  const int blk_lo = split * bps;
+  // blocks before the sliding window's left edge are never read
+  const int blk_lo = start / kDecBN + split * bps;
   const int blk_hi = min(nblk, blk_lo + bps);
   const int nb = max(0, blk_hi - blk_lo);
 
@@ -177,14 +180,15 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
     // ------------------------------ compute warps ------------------------------
     // (each register budget covers only its own role's code)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_COMPUTE));
-    compute_split<D, G, BF16>(p, smem, full, empty, red, warp, lane, split, bi, kvh, h_first, blk_lo, nb, limit);
+    compute_split<D, G, BF16>(p, smem, full, empty, red, warp, lane, split, bi, kvh, h_first, blk_lo, nb, start,
+                              limit);
   }
 }
 
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int warp, int lane, int split, int bi, int kvh,
-                                              int h_first, int blk_lo, int nb, int limit) {
+                                              int h_first, int blk_lo, int nb, int start, int limit) {
   using C = DecCfg<D>;
   using L = DecLane<D, G>;
   const int c = lane % L::LPR;      // dim group of this lane
@@ -220,16 +224,18 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     const uint8_t* vs = ks + C::KV_BYTES;
     const int key0 = (blk_lo + i) * kDecBN + warp * kDecRowsPerWarp;
     // the last block of a sequence may hold rows past its end (another sequence's
-    // keys, or cache slots never written): their V rows are zeroed below
-    const bool tail_block = (blk_lo + i + 1) * kDecBN > limit;
-    if (tail_block) {
-      // zero this warp's V rows past the end in shared memory (the TMA copy has
-      // landed: the full barrier was waited on), so the loop below stays as is
+    // keys, or cache slots never written), the first one rows before the window:
+    // their V rows are zeroed below
+    const bool edge_block = (blk_lo + i + 1) * kDecBN > limit || (blk_lo + i) * kDecBN < start;
+    if (edge_block) {
+      // zero this warp's V rows outside [start, limit) in shared memory (the TMA
+      // copy has landed: the full barrier was waited on), so the loop below stays as is
       uint8_t* vw = smem + slot * C::STAGE_BYTES + C::KV_BYTES;
 #pragma unroll
       for (int ps = 0; ps < L::PASSES; ++ps) {
         const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
-        if (key0 + ps * L::RPP + rg >= limit) {
+        const int key = key0 + ps * L::RPP + rg;
+        if (key >= limit || key < start) {
 #pragma unroll
           for (int sg = 0; sg < L::SEG; ++sg)
             *reinterpret_cast<uint4*>(vw + kr * (D * 2) + 2 * (sg * (D / L::SEG) + 8 * c)) = make_uint4(0u, 0u, 0u, 0u);
@@ -261,7 +267,7 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] += __shfl_xor_sync(0xffffffffu, sc[ps][h], x);
       const int key = key0 + ps * L::RPP + rg;
-      if (key >= limit) {
+      if (key >= limit || key < start) {
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] = -INFINITY;
       }

@@ -18,8 +18,10 @@ struct PrefillParams {
   float* o_part;     // split mode: normalised partial outputs [ns][b][hq][sq][d]
   int64_t o_stride_b, o_stride_row, o_stride_h;  // elements
   int b, sq, skv, hq, hkv, g;
-  int causal;
-  int off;             // row i sees key j iff j <= i + off (when causal)
+  int causal;          // right edge active: row i sees key j only if j <= i + off
+  int off;
+  int local;           // left edge active: row i sees key j only if j >= i + left_off
+  int left_off;
   float scale_log2;    // scale * log2(e)
   int n_mtiles;        // ceil(sq / 128)
   int n_mcta;          // ceil(n_mtiles / NQ)
@@ -47,7 +49,9 @@ struct DecodeParams {
   int nblk;          // ceil(skv / BN)
   int blocks_per_split;
   int num_splits;
-  int kv_limit;      // keys j < kv_limit are visible (min(skv, off + 1) when causal)
+  int kv_limit;      // dense: keys j < kv_limit are visible (min(skv, off + 1) when causal)
+  int kv_start;      // dense: keys j >= kv_start are visible (the sliding window's left edge)
+  int window_left;   // paged / packed: keys j >= len - 1 - window_left are visible; -1 = all
   float scale_log2;
   int* status;
   int kv_mode;                  // kKvDense, kKvPaged or kKvPacked

@@ -17,7 +17,9 @@
 //     accumulators in TMEM.
 // KV blocks are visited from the highest to the lowest index, so the blocks that
 // need the elementwise causal / tail mask come first; blocks past the causal
-// diagonal are never visited.
+// diagonal, or wholly outside the sliding window, are never visited (the
+// n_block_min / n_block_max rule of "flash attention V2 code walkthrough",
+// section 2, per Q tile).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -184,22 +186,31 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     n_cap = min(nblk_total, n_lo + p.blocks_per_split);
     if (n_lo > n_cap) n_lo = n_cap;
   }
-  int n_hi[NQ];
-  int n_hi_max = n_lo;
+  // Tile t visits the blocks [n_lo_t[t], n_hi[t]) (empty when equal); the CTA
+  // streams the union [n_lo_min, n_hi_max), which is contiguous because the
+  // tiles are adjacent row ranges.
+  int n_hi[NQ], n_lo_t[NQ];
+  int n_hi_max = n_lo, n_lo_min = n_cap;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) {
     const int row0 = (m_cta * NQ + t) * BM;
-    int hi = n_lo;
+    int lo = n_lo, hi = n_lo;
     if (row0 < p.sq) {
       const int last_row = min(row0 + BM, p.sq) - 1;
       hi = n_cap;
       if (p.causal) hi = min(hi, floor_div(last_row + p.off, BN) + 1);
-      hi = max(hi, n_lo);
+      if (p.local) lo = max(lo, floor_div(row0 + p.left_off, BN));
+      if (hi <= lo) hi = lo = n_lo;
     }
     n_hi[t] = hi;
-    n_hi_max = max(n_hi_max, hi);
+    n_lo_t[t] = lo;
+    if (hi > lo) {
+      n_hi_max = max(n_hi_max, hi);
+      n_lo_min = min(n_lo_min, lo);
+    }
   }
-  const int N = n_hi_max - n_lo;  // KV blocks visited by the CTA
+  if (n_lo_min > n_hi_max) n_lo_min = n_hi_max;
+  const int N = n_hi_max - n_lo_min;  // KV blocks visited by the CTA
 
   // ---- setup ----
   if (threadIdx.x == 0) {
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       const uint64_t pol_kv = l2_policy_evict_last();
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
-        if (n_hi[t] > n_lo) {
+        if (n_hi[t] > n_lo_t[t]) {
           mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < C::DC; ++c)
@@ -264,7 +275,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         if (!mbar_wait(&kv_full[L % C::STAGES], (L / C::STAGES) & 1, p.status, kSiteDrain)) break;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        if (n_hi[t] > n_lo) mbar_wait(&q_full[t], 0, p.status, kSiteDrain);
+        if (n_hi[t] > n_lo_t[t]) mbar_wait(&q_full[t], 0, p.status, kSiteDrain);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -278,11 +289,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);  // Q tile 0, K step 0
       const uint64_t k_desc = sdesc_sw128(ring_s, 16, 1024);          // slot 0 read as K (K-major)
       const uint64_t v_desc = sdesc_sw128(ring_s, BN * 128, 1024);    // slot 0 read as V (MN-major)
-      auto active = [&](int t, int it) { return n_hi_max - 1 - it < n_hi[t]; };
+      auto active = [&](int t, int it) {
+        const int n = n_hi_max - 1 - it;
+        return n < n_hi[t] && n >= n_lo_t[t];
+      };
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        if (ok && n_hi[t] > n_lo) ok = mbar_wait(&q_full[t], 0, p.status, kSiteQFull);
+        if (ok && n_hi[t] > n_lo_t[t]) ok = mbar_wait(&q_full[t], 0, p.status, kSiteQFull);
       int pv_count[NQ];
 #pragma unroll
       for (int t = 0; t < NQ; ++t) pv_count[t] = 0;
@@ -350,13 +364,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     const uint32_t tS = tbase + lane_off + Cfg<D>::s_col(t);
     const uint32_t tO = tbase + lane_off + Cfg<D>::o_col(t);
     const float sl2 = p.scale_log2;
-    // keys j < lim_row are visible to this row (the causal bound folded with the tail)
+    // keys lo_row <= j < lim_row are visible to this row (the causal / window
+    // edges folded with the tail)
     const int lim_row = p.causal ? min(p.skv, max(row + p.off + 1, 0)) : p.skv;
-    const int it0 = n_hi_max - n_hi[t];
+    const int lo_row = p.local ? row + p.left_off : 0;
+    // (selects, not a runtime index: the arrays stay in registers)
+    const int it0 = n_hi_max - (t == 0 ? n_hi[0] : n_hi[NQ - 1]);
+    const int it_end = n_hi_max - (t == 0 ? n_lo_t[0] : n_lo_t[NQ - 1]);
     float m_run = -INFINITY, l_run = 0.f;
     int k = 0;
     bool ok = true;
-    for (int it = it0; it < N; ++it) {
+    for (int it = it0; it < it_end; ++it) {
       const int n = n_hi_max - 1 - it;
       if (!warp_wait(&s_full[t], k & 1, p.status, kSiteSFull)) {
         ok = false;
@@ -381,6 +399,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c >= lim) s[c] = -INFINITY;
+      }
+      if (p.local && n * BN < row0 + BM - 1 + p.left_off) {
+        const int lo = lo_row - n * BN;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c < lo) s[c] = -INFINITY;
       }
       float mx[4];
 #pragma unroll
