@@ -57,7 +57,9 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* a head dimension or shape outside the compiled set */
   FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed */
   FA_ERR_TIMEOUT = 4,     /* a device-side wait gave up (reported by fa_sync_status) */
-  FA_ERR_SCRATCH_LIMIT = 5 /* fa_fwd_splitkv_noalloc: the problem does not fit the built-in scratch */
+  FA_ERR_SCRATCH_LIMIT = 5, /* fa_fwd_splitkv_noalloc: the problem does not fit the built-in scratch */
+  FA_ERR_DEVICE_ARG = 6     /* an argument read on the device (sequence offsets) failed its check
+                               (reported by fa_sync_status) */
 } fa_status;
 
 typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
@@ -219,6 +221,49 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits
 fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
                          int32_t* splits_used, void* stream);
 
+/*
+ * Forward pass over packed variable-length sequences ("flash attention V2 code
+ * walkthrough", Flash_fwd_params: cu_seqlens_q / cu_seqlens_k are prefix sums of
+ * the sequence lengths, e.g. [0, 248, 249, 250], and BlockInfo offsets each
+ * sequence's rows by them).  Sequence s owns query rows [cu_seqlens_q[s],
+ * cu_seqlens_q[s + 1]) of q / o and key rows [cu_seqlens_k[s], cu_seqlens_k[s + 1])
+ * of k / v; each sequence is an independent attention problem with the
+ * definition at the top of this file, its causal and window edges on its own
+ * bottom-right diagonal (q_pos_offset = its skv - its sq).  Same kernel as fa_fwd.
+ */
+typedef struct {
+  fa_dtype dtype;
+  int32_t b;                      /* sequences (>= 1) */
+  int32_t hq, hkv, d;             /* hq % hkv == 0; d in {64, 128, 256} */
+  int32_t total_q, total_k;       /* rows of the packed tensors (>= 0) */
+  int32_t max_seqlen_q;           /* host-side bound on every sequence's query rows (sizes the grid) */
+  const void* q;                  /* device, [total_q, hq, d] */
+  const void* k;                  /* device, [total_k, hkv, d] */
+  const void* v;                  /* device, [total_k, hkv, d] */
+  void* o;                        /* device, [total_q, hq, d], written */
+  float* lse;                     /* device, fp32 [hq, total_q], written */
+  int64_t q_strides[2];           /* (row, head) strides in elements, multiples of 8 */
+  int64_t k_strides[2];
+  int64_t v_strides[2];
+  int64_t o_strides[2];
+  const int32_t* cu_seqlens_q;    /* device, [b + 1], non-decreasing, cu[0] >= 0, cu[b] <= total_q */
+  const int32_t* cu_seqlens_k;    /* device, [b + 1], likewise with total_k */
+  int32_t causal;                 /* 0 or 1 */
+  int32_t local;                  /* 0 or 1: sliding window (widths as in fa_fwd_args, -1 = open side) */
+  int64_t window_left;
+  int64_t window_right;
+  float scale;                    /* finite, > 0 */
+} fa_varlen_args;
+
+/*
+ * Enqueue the packed variable-length forward pass.  The host checks what it can
+ * see; the prefix sums live on the device, so each CTA checks its sequence's
+ * offsets against total_q / total_k and max_seqlen_q before touching memory, skips
+ * the work if they are out of range and records FA_ERR_DEVICE_ARG for the next
+ * fa_sync_status (outputs of the rejected sequences are then left unwritten).
+ */
+fa_status fa_fwd_varlen(const fa_varlen_args* args, void* stream);
+
 /* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -255,8 +300,9 @@ fa_status fa_fwd_splitkv_noalloc(const fa_fwd_args* args, int32_t num_splits, in
 /*
  * Synchronise `stream` and report device-side failures on the current device:
  * FA_ERR_TIMEOUT if any kernel of this library recorded a wait that ran out
- * since the last call (the record is then cleared), FA_ERR_CUDA if the
- * synchronisation itself failed, FA_OK otherwise.
+ * since the last call, FA_ERR_DEVICE_ARG if a kernel rejected an argument it
+ * read on the device (the first record wins; it is then cleared), FA_ERR_CUDA if
+ * the synchronisation itself failed, FA_OK otherwise.
  */
 fa_status fa_sync_status(void* stream);
 

@@ -104,6 +104,7 @@ _LAYOUT_PROBE = r'''
 int main(void) {
   printf("fa_fwd_args size %zu\n", sizeof(fa_fwd_args));
   printf("fa_kvcache_args size %zu\n", sizeof(fa_kvcache_args));
+  printf("fa_varlen_args size %zu\n", sizeof(fa_varlen_args));
   FIELDS
   return 0;
 }
@@ -113,13 +114,14 @@ int main(void) {
 def test_ctypes_mirrors_match_header_layout(tmp_path):
     """Every field of the ctypes mirrors sits at the offset, with the size, that a C
     compiler gives the structs declared in include/fa.h."""
-    from tiled_exact_attention_gb300._lib import FwdArgs, KvcacheArgs
+    from tiled_exact_attention_gb300._lib import FwdArgs, KvcacheArgs, VarlenArgs
 
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
     fields = []
-    for cname, py in (("fa_fwd_args", FwdArgs), ("fa_kvcache_args", KvcacheArgs)):
+    mirrors = {"fa_fwd_args": FwdArgs, "fa_kvcache_args": KvcacheArgs, "fa_varlen_args": VarlenArgs}
+    for cname, py in mirrors.items():
         for name, _ in py._fields_:
             fields.append(f"F({cname}, {name})")
     src = tmp_path / "layout.c"
@@ -128,14 +130,14 @@ def test_ctypes_mirrors_match_header_layout(tmp_path):
     subprocess.run([gcc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
     sizes = {ln.split()[0]: int(ln.split()[2]) for ln in out if ln.split()[1] == "size"}
-    assert sizes["fa_fwd_args"] == ctypes.sizeof(FwdArgs)
-    assert sizes["fa_kvcache_args"] == ctypes.sizeof(KvcacheArgs)
+    for cname, py in mirrors.items():
+        assert sizes[cname] == ctypes.sizeof(py), cname
     for ln in out:
         parts = ln.split()
         if parts[1] == "size":
             continue
         struct, name, off, size = parts[0], parts[1], int(parts[2]), int(parts[3])
-        py = FwdArgs if struct == "fa_fwd_args" else KvcacheArgs
+        py = mirrors[struct]
         desc = getattr(py, name)
         assert (desc.offset, desc.size) == (off, size), (struct, name)
 
@@ -198,3 +200,44 @@ def test_kvcache_packed_needs_prefix_sums(lib):
     assert lib.fa_fwd_kvcache(ctypes.byref(a), 1, None, 0, None, None) == 1
     a = _kv_args(page_size=0, cu_seqlens_k=4096)
     assert lib.fa_kvcache_workspace_size(ctypes.byref(a), 3) >= 3 * 2 * 8 * (128 + 1) * 4
+
+
+def _varlen_args(**kw):
+    from tiled_exact_attention_gb300._lib import VarlenArgs
+
+    a = VarlenArgs()
+    a.dtype, a.b, a.hq, a.hkv, a.d = 0, 2, 4, 2, 128
+    a.total_q, a.total_k, a.max_seqlen_q = 300, 400, 200
+    a.q = a.k = a.v = a.o = 4096
+    a.lse = a.cu_seqlens_q = a.cu_seqlens_k = 4096
+    a.q_strides = (ctypes.c_int64 * 2)(4 * 128, 128)
+    a.o_strides = (ctypes.c_int64 * 2)(4 * 128, 128)
+    a.k_strides = (ctypes.c_int64 * 2)(2 * 128, 128)
+    a.v_strides = (ctypes.c_int64 * 2)(2 * 128, 128)
+    a.scale = 0.1
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("dtype", 3, 1), ("b", 0, 1), ("hq", 3, 1), ("d", 96, 2), ("total_q", -1, 1), ("max_seqlen_q", -1, 1),
+    ("causal", 2, 1), ("local", 2, 1), ("scale", 0.0, 1), ("q", 0, 1), ("cu_seqlens_q", 0, 1),
+    ("cu_seqlens_k", 4098, 1), ("k", 4100, 1), ("lse", 0, 1), ("total_k", (1 << 30) + 1, 2),
+])
+def test_varlen_validation(lib, field, value, expect):
+    a = _varlen_args(**{field: value})
+    assert lib.fa_fwd_varlen(ctypes.byref(a), None) == expect
+
+
+def test_varlen_validation_strides_and_empty(lib):
+    a = _varlen_args()
+    a.q_strides = (ctypes.c_int64 * 2)(4 * 128, 100)
+    assert lib.fa_fwd_varlen(ctypes.byref(a), None) == 1
+    a = _varlen_args(local=1, window_left=-3, window_right=0)
+    assert lib.fa_fwd_varlen(ctypes.byref(a), None) == 1
+    assert lib.fa_fwd_varlen(None, None) == 1
+    # nothing to compute: no launch, no device needed
+    assert lib.fa_fwd_varlen(ctypes.byref(_varlen_args(total_q=0)), None) == 0
+    assert lib.fa_fwd_varlen(ctypes.byref(_varlen_args(max_seqlen_q=0)), None) == 0
+    assert lib.fa_status_string(6) == b"an argument read on the device (sequence offsets) failed its check"

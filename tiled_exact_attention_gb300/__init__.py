@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     fa_fwd_kvcache,
     fa_fwd_splitkv,
     fa_fwd_splitkv_noalloc,
+    fa_fwd_varlen,
     fa_num_splits_heuristic,
     fa_selftest_wait_timeout,
     fa_splitkv_combine,

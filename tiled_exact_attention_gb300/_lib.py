@@ -14,6 +14,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_SCRATCH_LIMIT = 5
+FA_ERR_DEVICE_ARG = 6
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 FA_BF16 = 0
@@ -31,6 +32,7 @@ EXPORTS = (
     "fa_fwd_splitkv_noalloc",
     "fa_kvcache_workspace_size",
     "fa_fwd_kvcache",
+    "fa_fwd_varlen",
     "fa_splitkv_combine",
     "fa_sync_status",
     "fa_selftest_wait_timeout",
@@ -99,6 +101,37 @@ class KvcacheArgs(ctypes.Structure):
     ]
 
 
+class VarlenArgs(ctypes.Structure):
+    """Mirror of `fa_varlen_args`."""
+
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("b", ctypes.c_int32),
+        ("hq", ctypes.c_int32),
+        ("hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("total_q", ctypes.c_int32),
+        ("total_k", ctypes.c_int32),
+        ("max_seqlen_q", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("q_strides", ctypes.c_int64 * 2),
+        ("k_strides", ctypes.c_int64 * 2),
+        ("v_strides", ctypes.c_int64 * 2),
+        ("o_strides", ctypes.c_int64 * 2),
+        ("cu_seqlens_q", ctypes.c_void_p),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("causal", ctypes.c_int32),
+        ("local", ctypes.c_int32),
+        ("window_left", ctypes.c_int64),
+        ("window_right", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+    ]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -139,6 +172,8 @@ def load():
         lib.fa_kvcache_workspace_size.restype = ctypes.c_size_t
         lib.fa_fwd_kvcache.argtypes = [pkv, i32, vp, ctypes.c_size_t, ctypes.POINTER(i32), vp]
         lib.fa_fwd_kvcache.restype = ctypes.c_int
+        lib.fa_fwd_varlen.argtypes = [ctypes.POINTER(VarlenArgs), vp]
+        lib.fa_fwd_varlen.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

@@ -13,7 +13,7 @@ import math
 import torch
 
 from . import _lib
-from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, KvcacheArgs, check
+from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, KvcacheArgs, VarlenArgs, check
 
 _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
@@ -210,6 +210,63 @@ def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=No
                              _stream_handle(stream)), "fa_fwd_kvcache")
     if return_splits:
         return out, lse, int(used.value)
+    return out, lse
+
+
+def make_varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, causal: bool,
+                     scale: float | None, window=None) -> VarlenArgs:
+    """Fill `fa_varlen_args`.  q, o: [total_q, hq, d]; k, v: [total_k, hkv, d]; lse: fp32 [hq, total_q];
+    cu_seqlens_q / cu_seqlens_k: CUDA int32 [b + 1] prefix sums."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", o)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in _DT or t.dim() != 3 \
+                or t.stride(2) != 1:
+            raise ValueError(f"{name} must be a CUDA bf16/fp16 [rows, heads, d] tensor with contiguous d")
+    if q.dtype != k.dtype or q.dtype != v.dtype or o.dtype != q.dtype:
+        raise ValueError("q, k, v, out must share a dtype")
+    if k.shape != v.shape or q.shape[2] != k.shape[2] or o.shape != q.shape:
+        raise ValueError("inconsistent q/k/v/out shapes")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA int32 vector")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold b + 1 >= 2 entries")
+    total_q, hq, d = q.shape
+    total_k, hkv = k.shape[0], k.shape[1]
+    if lse.shape != (hq, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [hq, total_q]")
+    a = VarlenArgs()
+    a.dtype = _DT[q.dtype]
+    a.b = cu_seqlens_q.numel() - 1
+    a.hq, a.hkv, a.d = hq, hkv, d
+    a.total_q, a.total_k, a.max_seqlen_q = total_q, total_k, int(max_seqlen_q)
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+    a.q_strides = (ctypes.c_int64 * 2)(q.stride(0), q.stride(1))
+    a.k_strides = (ctypes.c_int64 * 2)(k.stride(0), k.stride(1))
+    a.v_strides = (ctypes.c_int64 * 2)(v.stride(0), v.stride(1))
+    a.o_strides = (ctypes.c_int64 * 2)(o.stride(0), o.stride(1))
+    a.cu_seqlens_q, a.cu_seqlens_k = cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr()
+    a.causal = 1 if causal else 0
+    if window is not None:
+        a.local = 1
+        a.window_left, a.window_right = int(window[0]), int(window[1])
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    return a
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int | None = None, causal: bool = False,
+                  scale: float | None = None, window=None, out=None, lse=None, stream=None):
+    """Forward pass over packed variable-length sequences; returns (O [total_q, hq, d], LSE [hq, total_q]).
+    max_seqlen_q defaults to the longest sequence (read back from the device once)."""
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    if max_seqlen_q is None:
+        lens = cu_seqlens_q[1:] - cu_seqlens_q[:-1]
+        max_seqlen_q = int(lens.max().item()) if lens.numel() else 0
+    a = make_varlen_args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=max_seqlen_q, causal=causal,
+                         scale=scale, window=window)
+    check(_lib.load().fa_fwd_varlen(ctypes.byref(a), _stream_handle(stream)), "fa_fwd_varlen")
     return out, lse
 
 

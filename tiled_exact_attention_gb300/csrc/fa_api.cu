@@ -2,6 +2,7 @@
 // tensor-map encoding, the split-count heuristic, launches and status codes.
 // No allocation happens here: every buffer, including the split-KV workspace,
 // belongs to the caller.
+#include <array>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -9,6 +10,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace {
@@ -263,6 +265,40 @@ fa_status validate_kvcache(const fa_kvcache_args* a) {
   return FA_OK;
 }
 
+bool strides2_ok(const int64_t s[2]) {
+  for (int i = 0; i < 2; ++i) {
+    if (s[i] <= 0 || (s[i] % 8) != 0) return false;
+    if (s[i] * 2 >= (static_cast<int64_t>(1) << 40)) return false;
+  }
+  return true;
+}
+
+fa_status validate_varlen(const fa_varlen_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
+  if (a->total_q < 0 || a->total_k < 0 || a->max_seqlen_q < 0) return FA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return FA_ERR_INVALID_ARG;
+  if (a->local != 0 && a->local != 1) return FA_ERR_INVALID_ARG;
+  if (a->local && (a->window_left < -1 || a->window_right < -1)) return FA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
+  if (a->total_q > (1 << 30) || a->total_k > (1 << 30) || a->max_seqlen_q > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (a->total_q == 0 || a->max_seqlen_q == 0) return FA_OK;
+  if (a->q == nullptr || a->o == nullptr || a->lse == nullptr || a->cu_seqlens_q == nullptr ||
+      a->cu_seqlens_k == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4) || !aligned(a->cu_seqlens_q, 4) ||
+      !aligned(a->cu_seqlens_k, 4))
+    return FA_ERR_INVALID_ARG;
+  if (!strides2_ok(a->q_strides) || !strides2_ok(a->o_strides)) return FA_ERR_INVALID_ARG;
+  if (a->total_k > 0) {
+    if (a->k == nullptr || a->v == nullptr || !aligned(a->k, 16) || !aligned(a->v, 16)) return FA_ERR_INVALID_ARG;
+    if (!strides2_ok(a->k_strides) || !strides2_ok(a->v_strides)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
 int kvcache_splits(const fa_kvcache_args* a, int32_t requested, const DeviceInfo& di) {
   const int g = a->hq / a->hkv;
   const int64_t units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
@@ -304,6 +340,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "device-side wait timed out";
     case FA_ERR_SCRATCH_LIMIT: return "problem needs more split-KV scratch than the built-in buffer holds";
+    case FA_ERR_DEVICE_ARG: return "an argument read on the device (sequence offsets) failed its check";
     default: return "unknown status";
   }
 }
@@ -581,6 +618,67 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* a, int32_t num_splits) {
   return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
 }
 
+fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
+  const fa_status v = validate_varlen(a);
+  if (v != FA_OK || a->total_q == 0 || a->max_seqlen_q == 0) return v;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int bn = prefill_block_n(a->d);
+  // 4-D views (d, h, total, 1) of the packed tensors
+  auto st3 = [](const int64_t s2[2], int64_t total) {
+    return std::array<int64_t, 3>{s2[0] * (total > 0 ? total : 1), s2[0], s2[1]};
+  };
+  const auto qs = st3(a->q_strides, a->total_q), os = st3(a->o_strides, a->total_q);
+  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->total_q, 1, qs.data(), 64, 128, true) ||
+      !encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->total_q, 1, os.data(), 64, 128, true))
+    return FA_ERR_INVALID_ARG;
+  if (a->total_k > 0) {
+    const auto ks = st3(a->k_strides, a->total_k), vs = st3(a->v_strides, a->total_k);
+    if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->total_k, 1, ks.data(), 64, bn, true) ||
+        !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->total_k, 1, vs.data(), 64, bn, true))
+      return FA_ERR_INVALID_ARG;
+  }
+  // Mask edges relative to each sequence's diagonal (the kernel adds skv - sq).
+  constexpr int64_t kEdge = static_cast<int64_t>(1) << 30;
+  p.causal = 0;
+  p.off = 0;
+  if (a->causal || (a->local && a->window_right >= 0)) {
+    int64_t off = kEdge;
+    if (a->causal) off = 0;
+    if (a->local && a->window_right >= 0 && a->window_right < off) off = a->window_right;
+    p.causal = 1;
+    p.off = static_cast<int>(off);
+  }
+  if (a->local && a->window_left >= 0) {
+    p.local = 1;
+    p.left_off = static_cast<int>(-(a->window_left < kEdge ? a->window_left : kEdge));
+  }
+  p.o = a->o;
+  p.lse = a->lse;
+  p.o_stride_b = 0;
+  p.o_stride_row = a->o_strides[0];
+  p.o_stride_h = a->o_strides[1];
+  p.b = a->b;
+  p.sq = a->max_seqlen_q;
+  p.skv = 0;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  p.n_mtiles = static_cast<int>(ceil_div64(a->max_seqlen_q, 128));
+  p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+  p.num_splits = 1;
+  p.blocks_per_split = 0;
+  p.status = di.status;
+  p.cu_q = a->cu_seqlens_q;
+  p.cu_k = a->cu_seqlens_k;
+  p.total_q = a->total_q;
+  p.total_k = a->total_k;
+  return from_cuda(launch_prefill(p, a->d, a->dtype, static_cast<cudaStream_t>(stream)));
+}
+
 fa_status fa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   DeviceInfo di;
@@ -590,7 +688,7 @@ fa_status fa_sync_status(void* stream) {
   if (code != 0) {
     const int zero = 0;
     if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    return code == kErrDeviceArg ? FA_ERR_DEVICE_ARG : FA_ERR_TIMEOUT;
   }
   return FA_OK;
 }

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
         ++issued;
       }
       for (int i = max(0, issued - C::STAGES); i < issued; ++i)
-        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, p.status, kSiteDecDrain)) break;
+        if (!mbar_wait(&full[i % C::STAGES], (i / C::STAGES) & 1, p.status, kSiteDecDrain, true)) break;
     }
     __syncwarp();
     __syncthreads();

@@ -28,6 +28,13 @@ struct PrefillParams {
   int num_splits;      // 1 = plain forward
   int blocks_per_split;
   int* status;
+  // Packed variable-length sequences (null for the dense layout): Q/O rows of
+  // sequence b are [cu_q[b], cu_q[b + 1]), K/V rows [cu_k[b], cu_k[b + 1]); the
+  // tensor maps then cover [total][h][d] with one outer entry, sq is the longest
+  // sequence, and off / left_off are relative to each sequence's diagonal.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
 };
 
 // Where the decode kernel finds a sequence's keys.

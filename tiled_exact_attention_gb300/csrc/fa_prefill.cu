@@ -149,7 +149,9 @@ __device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, 
   }
 }
 
-template <int D, bool BF16>
+// VARLEN: packed variable-length sequences (p.cu_q / p.cu_k); a separate
+// instantiation so that the dense kernel keeps its sizes in the constant bank.
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
@@ -179,7 +181,33 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
   const int h = bh % p.hq, bi = bh / p.hq;
   const int kvh = h / p.g;
 
-  const int nblk_total = (p.skv + BN - 1) / BN;
+  // ---- the sequence: one batch entry, or one packed variable-length sequence ----
+  // Packed: sequence bi owns Q rows [cu_q[bi], cu_q[bi + 1]) and K/V rows
+  // [cu_k[bi], cu_k[bi + 1]); its mask edges sit on its own bottom-right
+  // diagonal (the host passes them relative to that diagonal).
+  int sq = p.sq, skv = p.skv, off = p.off, left_off = p.left_off;
+  int q_base = 0, k_base = 0, tb = bi;  // row offsets and batch coordinate in the tensor maps
+  if constexpr (VARLEN) {
+    q_base = p.cu_q[bi];
+    sq = p.cu_q[bi + 1] - q_base;
+    k_base = p.cu_k[bi];
+    skv = p.cu_k[bi + 1] - k_base;
+    tb = 0;
+    const bool ok_seq = q_base >= 0 && sq >= 0 && q_base <= p.total_q - sq && k_base >= 0 && skv >= 0 &&
+                        k_base <= p.total_k - skv && sq <= p.n_mtiles * BM;
+    if (!ok_seq) {
+      // nothing of this CTA has started: no copy, barrier or TMEM to release
+      if (threadIdx.x == 0) record_error(p.status, kErrDeviceArg);
+      return;
+    }
+    if ((m_cta * NQ) * BM >= sq) return;  // no row of this sequence here
+    const int64_t diag = static_cast<int64_t>(skv) - sq;
+    const int64_t o64 = diag + p.off, l64 = diag + p.left_off;
+    off = static_cast<int>(o64 < -sq - 1 ? -sq - 1 : (o64 > skv ? skv : o64));
+    left_off = static_cast<int>(l64 < -sq ? -sq : (l64 > skv ? skv : l64));
+  }
+
+  const int nblk_total = (skv + BN - 1) / BN;
   int n_lo = 0, n_cap = nblk_total;
   if (p.num_splits > 1) {
     n_lo = split * p.blocks_per_split;
@@ -195,11 +223,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
   for (int t = 0; t < NQ; ++t) {
     const int row0 = (m_cta * NQ + t) * BM;
     int lo = n_lo, hi = n_lo;
-    if (row0 < p.sq) {
-      const int last_row = min(row0 + BM, p.sq) - 1;
+    if (row0 < sq) {
+      const int last_row = min(row0 + BM, sq) - 1;
       hi = n_cap;
-      if (p.causal) hi = min(hi, floor_div(last_row + p.off, BN) + 1);
-      if (p.local) lo = max(lo, floor_div(row0 + p.left_off, BN));
+      if (p.causal) hi = min(hi, floor_div(last_row + off, BN) + 1);
+      if (p.local) lo = max(lo, floor_div(row0 + left_off, BN));
       if (hi <= lo) hi = lo = n_lo;
     }
     n_hi[t] = hi;
@@ -254,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 #pragma unroll
           for (int c = 0; c < C::DC; ++c)
             tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, &q_full[t], c * 64, h,
-                        (m_cta * NQ + t) * BM, bi);
+                        q_base + (m_cta * NQ + t) * BM, tb);
         }
       }
       int issued = 0;
@@ -266,16 +294,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < C::DC; ++c)
-          tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * 64, kvh, n * BN,
-                           bi, pol_kv);
+          tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * 64, kvh,
+                           k_base + n * BN, tb, pol_kv);
         ++issued;
       }
       // No copy may still be in flight when the CTA leaves: wait for the last ones.
       for (int L = max(0, issued - C::STAGES); L < issued; ++L)
-        if (!mbar_wait(&kv_full[L % C::STAGES], (L / C::STAGES) & 1, p.status, kSiteDrain)) break;
+        if (!mbar_wait(&kv_full[L % C::STAGES], (L / C::STAGES) & 1, p.status, kSiteDrain, true)) break;
 #pragma unroll
       for (int t = 0; t < NQ; ++t)
-        if (n_hi[t] > n_lo_t[t]) mbar_wait(&q_full[t], 0, p.status, kSiteDrain);
+        if (n_hi[t] > n_lo_t[t]) mbar_wait(&q_full[t], 0, p.status, kSiteDrain, true);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -366,8 +394,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     const float sl2 = p.scale_log2;
     // keys lo_row <= j < lim_row are visible to this row (the causal / window
     // edges folded with the tail)
-    const int lim_row = p.causal ? min(p.skv, max(row + p.off + 1, 0)) : p.skv;
-    const int lo_row = p.local ? row + p.left_off : 0;
+    const int lim_row = p.causal ? min(skv, max(row + off + 1, 0)) : skv;
+    const int lo_row = p.local ? row + left_off : 0;
     // (selects, not a runtime index: the arrays stay in registers)
     const int it0 = n_hi_max - (t == 0 ? n_hi[0] : n_hi[NQ - 1]);
     const int it_end = n_hi_max - (t == 0 ? n_lo_t[0] : n_lo_t[NQ - 1]);
@@ -393,14 +421,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       uint32_t sr[BN];
       tmem_load_row<BN>(tS, sr);
       float* s = reinterpret_cast<float*>(sr);
-      const bool masked = (n + 1) * BN > p.skv || (p.causal && (n + 1) * BN - 1 > row0 + p.off);
+      const bool masked = (n + 1) * BN > skv || (p.causal && (n + 1) * BN - 1 > row0 + off);
       if (masked) {
         const int lim = lim_row - n * BN;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      if (p.local && n * BN < row0 + BM - 1 + p.left_off) {
+      if (p.local && n * BN < row0 + BM - 1 + left_off) {
         const int lo = lo_row - n * BN;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -480,21 +508,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 
     // ---------------- epilogue ----------------
     const bool split_mode = p.num_splits > 1;
+    // LSE [b][hq][sq], or [hq][total_q] for packed sequences
+    const int64_t lse_idx = VARLEN ? static_cast<int64_t>(h) * p.total_q + q_base + row
+                                   : (static_cast<int64_t>(bi) * p.hq + h) * sq + row;
+    uint16_t* o_row = static_cast<uint16_t*>(p.o) + bi * p.o_stride_b +
+                      static_cast<int64_t>(q_base + row) * p.o_stride_row + h * p.o_stride_h;
     if (ok && k == 0) {
       // This tile sees no key (in this split): O = 0, LSE = -inf.
-      if (row < p.sq) {
+      if (row < sq) {
         if (split_mode) {
-          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * p.sq + row;
+          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * sq + row;
           float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
           for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
           p.lse[prow] = -INFINITY;
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + bi * p.o_stride_b +
-                                                static_cast<int64_t>(row) * p.o_stride_row + h * p.o_stride_h);
+          uint4* dst = reinterpret_cast<uint4*>(o_row);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[(static_cast<int64_t>(bi) * p.hq + h) * p.sq + row] = -INFINITY;
+          p.lse[lse_idx] = -INFINITY;
         }
       }
     } else if (ok) {
@@ -505,8 +537,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         if (split_mode) {
           // The TMEM loads are warp-collective: every lane executes them and only
           // the global stores depend on whether the row exists.
-          const bool valid = row < p.sq;
-          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * p.sq + row;
+          const bool valid = row < sq;
+          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * sq + row;
           float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
           for (int c = 0; c < D; c += 32) {
@@ -520,6 +552,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
             }
           }
           if (valid) p.lse[prow] = lse;
+        } else if (VARLEN && row0 + BM > sq) {
+          // The last tile of a packed sequence: a 128-row TMA store would also write
+          // the next sequence's rows, so each thread stores its own row.
+          const bool valid = row < sq;
+          uint4* dst = reinterpret_cast<uint4*>(o_row);
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_load_row<32>(tO + c, o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (valid) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[c / 8 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+          }
+          if (valid) p.lse[lse_idx] = lse;
         } else {
           // Stage O (normalised, rounded) through the Q tile's shared memory in the
           // same 128-byte-swizzled layout the TMA store reads.
@@ -545,11 +597,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
           named_bar_sync(1 + t, BM);
           if (r == 0) {
 #pragma unroll
-            for (int cc = 0; cc < C::DC; ++cc) tma_store_4d(&p.tm_o, stage + cc * (BM * 128), cc * 64, h, row0, bi);
+            for (int cc = 0; cc < C::DC; ++cc)
+              tma_store_4d(&p.tm_o, stage + cc * (BM * 128), cc * 64, h, q_base + row0, tb);
             bulk_commit_group();
             bulk_wait_group_read0();
           }
-          if (row < p.sq) p.lse[(static_cast<int64_t>(bi) * p.hq + h) * p.sq + row] = lse;
+          if (row < sq) p.lse[lse_idx] = lse;
         }
       }
     }
@@ -566,7 +619,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = fa_prefill_kernel<D, BF16>;
+  auto kern = p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;

@@ -21,6 +21,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 enum : int {
   kErrNone = 0,
   kErrTimeoutBase = 0x100,  // + site id
+  kErrDeviceArg = 0x200,    // an argument read on the device (sequence offsets) failed its check
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -33,8 +34,10 @@ __device__ __forceinline__ void record_error(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// True once some wait of the grid has timed out (other waits then give up early;
+// a device-side argument error does not stop the CTAs that are unaffected by it).
 __device__ __forceinline__ bool error_pending(const int* status) {
-  return status != nullptr && *reinterpret_cast<const volatile int*>(status) != 0;
+  return status != nullptr && (*reinterpret_cast<const volatile int*>(status) & kErrTimeoutBase) != 0;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -74,16 +77,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// records `kErrTimeoutBase + site`) when the wait exceeds kWaitLimitNs or when
-// another thread of the grid has already recorded an error.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int site) {
+// records `kErrTimeoutBase + site`) when the wait exceeds kWaitLimitNs or, unless
+// `drain` is set, when another wait of the grid has already timed out.  Waits for
+// a CTA's own copies in flight pass drain = true: those complete by themselves,
+// and the CTA must not leave before they land.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int site,
+                                          bool drain = false) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (error_pending(status)) return false;
+      if (!drain && error_pending(status)) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
         record_error(status, kErrTimeoutBase + site);
         return false;
