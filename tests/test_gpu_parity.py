@@ -124,6 +124,25 @@ def test_permuted_layout_matches_contiguous():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_output_only_16_byte_aligned(d):
+    """An output whose base and row stride are 16- but not 32-byte aligned takes the
+    16-byte store path; same result as a contiguous output."""
+    b, s, h = 1, 300, 2
+    q, k, v = _cuda(*make_custom(b, s, s, h, h, d, "bf16", seed=79))
+    o1, l1 = fa_fwd(q, k, v, causal=True)
+    row = h * d + 8  # elements: a multiple of 8 but not of 16
+    buf = torch.full((b * s * row + 8,), 3.0, dtype=torch.bfloat16, device=DEV)
+    o2 = buf[8:].as_strided((b, s, h, d), (s * row, row, d, 1))
+    assert o2.data_ptr() % 32 == 16
+    fa_fwd(q, k, v, causal=True, out=o2)
+    assert fa_sync_status() == 0
+    assert torch.equal(o1, o2)
+    # the 8 padding elements of each row are untouched
+    pad = buf[8:].view(b * s, row)[:, h * d:]
+    assert torch.all(pad == 3.0)
+
+
 def test_deterministic():
     q, k, v = _cuda(*make_custom(1, 640, 640, 4, 4, 128, "bf16", seed=5))
     o1, l1 = fa_fwd(q, k, v, causal=True)

@@ -368,8 +368,7 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
   const int bn = prefill_block_n(a->d);
-  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->sq, a->b, a->q_strides, 64, 128, true) ||
-      !encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->sq, a->b, a->o_strides, 64, 128, true))
+  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->sq, a->b, a->q_strides, 64, 128, true))
     return FA_ERR_INVALID_ARG;
   if (a->skv > 0 &&
       (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
@@ -382,6 +381,8 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   p.o_stride_b = a->o_strides[0];
   p.o_stride_row = a->o_strides[1];
   p.o_stride_h = a->o_strides[2];
+  p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0 &&
+              a->o_strides[2] % 16 == 0;
   p.b = a->b;
   p.sq = a->sq;
   p.skv = a->skv;
@@ -397,6 +398,7 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
   p.num_splits = 1;
   p.blocks_per_split = static_cast<int>(ceil_div64(a->skv, bn));
+  p.max_ctas = di.sms;
   p.status = di.status;
   return from_cuda(launch_prefill(p, a->d, a->dtype, static_cast<cudaStream_t>(stream)));
 }
@@ -525,6 +527,7 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     p.num_splits = ns;
     const int64_t nblk = ceil_div64(a->skv, bn);
     p.blocks_per_split = static_cast<int>(ceil_div64(nblk > 0 ? nblk : 1, ns));
+    p.max_ctas = di.sms;
     p.status = di.status;
     e = launch_prefill(p, a->d, a->dtype, st);
   }
@@ -630,9 +633,8 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   auto st3 = [](const int64_t s2[2], int64_t total) {
     return std::array<int64_t, 3>{s2[0] * (total > 0 ? total : 1), s2[0], s2[1]};
   };
-  const auto qs = st3(a->q_strides, a->total_q), os = st3(a->o_strides, a->total_q);
-  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->total_q, 1, qs.data(), 64, 128, true) ||
-      !encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->total_q, 1, os.data(), 64, 128, true))
+  const auto qs = st3(a->q_strides, a->total_q);
+  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->total_q, 1, qs.data(), 64, 128, true))
     return FA_ERR_INVALID_ARG;
   if (a->total_k > 0) {
     const auto ks = st3(a->k_strides, a->total_k), vs = st3(a->v_strides, a->total_k);
@@ -660,6 +662,7 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   p.o_stride_b = 0;
   p.o_stride_row = a->o_strides[0];
   p.o_stride_h = a->o_strides[1];
+  p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0;
   p.b = a->b;
   p.sq = a->max_seqlen_q;
   p.skv = 0;
@@ -671,6 +674,7 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
   p.num_splits = 1;
   p.blocks_per_split = 0;
+  p.max_ctas = di.sms;
   p.status = di.status;
   p.cu_q = a->cu_seqlens_q;
   p.cu_k = a->cu_seqlens_k;

@@ -12,11 +12,11 @@ struct PrefillParams {
   CUtensorMap tm_q;  // Q  [b][sq][hq][d],  box {64, 1, 128, 1}
   CUtensorMap tm_k;  // K  [b][skv][hkv][d], box {64, 1, BN, 1}
   CUtensorMap tm_v;  // V  same as K
-  CUtensorMap tm_o;  // O  same as Q (unused in split mode)
-  void* o;           // O base (empty tiles are written directly)
+  void* o;           // O base (written row by row by the softmax threads)
   float* lse;        // LSE [b][hq][sq] (or LSE partials [ns][b][hq][sq] in split mode)
   float* o_part;     // split mode: normalised partial outputs [ns][b][hq][sq][d]
   int64_t o_stride_b, o_stride_row, o_stride_h;  // elements
+  int o_vec32;         // O rows may be written with 32-byte stores (base and strides 32-byte aligned)
   int b, sq, skv, hq, hkv, g;
   int causal;          // right edge active: row i sees key j only if j <= i + off
   int off;
@@ -27,6 +27,7 @@ struct PrefillParams {
   int n_mcta;          // ceil(n_mtiles / NQ)
   int num_splits;      // 1 = plain forward
   int blocks_per_split;
+  int max_ctas;        // grid bound of the persistent kernel (the SM count)
   int* status;
   // Packed variable-length sequences (null for the dense layout): Q/O rows of
   // sequence b are [cu_q[b], cu_q[b + 1]), K/V rows [cu_k[b], cu_k[b + 1]); the

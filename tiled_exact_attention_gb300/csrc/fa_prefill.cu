@@ -51,7 +51,7 @@ struct Cfg {
   static constexpr int O_COL0 = 256;
   static constexpr int RING_OFF = NQ * Q_BYTES;
   static constexpr int BAR_OFF = RING_OFF + STAGES * KV_BYTES;
-  static constexpr int NUM_BARS = 4 * NQ + 2 * STAGES;
+  static constexpr int NUM_BARS = 3 + 4 * NQ + 2 * STAGES;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;
   // Register split (NQ == 2): launched at 168 per thread (384 threads), the
   // control warpgroup drops to 72 and the two softmax warpgroups rise to 216:
@@ -67,7 +67,17 @@ struct Cfg {
 };
 
 // Wait sites (recorded in the status word on timeout).
-enum : int { kSiteKvEmpty = 1, kSiteQFull, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain };
+enum : int {
+  kSiteKvEmpty = 1,
+  kSiteQFull,
+  kSiteKvFull,
+  kSitePFull,
+  kSiteSFull,
+  kSiteOFull,
+  kSiteDrain,
+  kSiteQEmpty,
+  kSiteOEmpty
+};
 
 __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
@@ -127,8 +137,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // K-major with 128-byte swizzle (64-column chunks of 128-byte rows).
 template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID>
 __device__ __forceinline__ void issue_s_tile(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int t, int slot) {
-  const uint64_t qd = q_desc + static_cast<uint32_t>((t * Q_BYTES) >> 4);
-  const uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  uint64_t qd = q_desc + static_cast<uint32_t>((t * Q_BYTES) >> 4);
+  uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  // opaque to the optimiser: the per-step descriptors are formed at issue time
+  // instead of being hoisted (and held in registers) across the item loop
+  asm volatile("" : "+l"(qd), "+l"(kd));
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
@@ -142,15 +155,119 @@ __device__ __forceinline__ void issue_s_tile(uint32_t d_tmem, uint64_t q_desc, u
 // bytes apart, 8-row groups 1024 bytes apart).
 template <int D, int BN, int KV_BYTES, uint32_t ID, int K0, int K1>
 __device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, int slot, bool acc) {
-  const uint64_t vd = v_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  uint64_t vd = v_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  asm volatile("" : "+l"(vd));
 #pragma unroll
   for (int k = K0; k < K1; ++k) {
     umma_ts(o_tmem, p_tmem + k * 8, vd + static_cast<uint32_t>((k * 2048) >> 4), ID, (acc || k > 0) ? 1u : 0u);
   }
 }
 
+// One work item: NQ Q tiles of one (split, batch or packed sequence, head) and
+// the key-block ranges they visit.  Every role derives the same plan from the
+// item index, so the roles need no channel to agree on it.
+template <int NQ>
+struct ItemPlan {
+  int bi, h, kvh, m_cta, split;
+  int sq, skv, off, left_off;  // the sequence's sizes and mask edges
+  int q_base, k_base, tb;      // packed row offsets; batch coordinate of the tensor maps
+  int n_hi[NQ], n_lo_t[NQ];    // tile t visits key blocks [n_lo_t[t], n_hi[t])
+  int n_hi_max;                // the CTA streams blocks n_hi_max - 1 down to n_hi_max - N
+  int N;
+  bool valid;                  // false: packed offsets out of range (nothing is touched)
+};
+
+template <int D, bool VARLEN>
+__device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p, int item) {
+  using C = Cfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
+  ItemPlan<NQ> w;
+  // Items are numbered longest causal row-group first (longest-processing-time
+  // order balances the SMs best; grouping work by head measured slower).
+  int idx = item;
+  w.split = idx % p.num_splits;
+  idx /= p.num_splits;
+  const int bh = idx % (p.b * p.hq);
+  w.m_cta = p.n_mcta - 1 - idx / (p.b * p.hq);
+  w.h = bh % p.hq;
+  w.bi = bh / p.hq;
+  w.kvh = w.h / p.g;
+  w.sq = p.sq;
+  w.skv = p.skv;
+  w.off = p.off;
+  w.left_off = p.left_off;
+  w.q_base = 0;
+  w.k_base = 0;
+  w.tb = w.bi;
+  w.valid = true;
+  if constexpr (VARLEN) {
+    // Packed: sequence bi owns Q rows [cu_q[bi], cu_q[bi + 1]) and K/V rows
+    // [cu_k[bi], cu_k[bi + 1]); its mask edges sit on its own bottom-right
+    // diagonal (the host passes them relative to that diagonal).
+    w.q_base = p.cu_q[w.bi];
+    w.sq = p.cu_q[w.bi + 1] - w.q_base;
+    w.k_base = p.cu_k[w.bi];
+    w.skv = p.cu_k[w.bi + 1] - w.k_base;
+    w.tb = 0;
+    w.valid = w.q_base >= 0 && w.sq >= 0 && w.q_base <= p.total_q - w.sq && w.k_base >= 0 && w.skv >= 0 &&
+              w.k_base <= p.total_k - w.skv && w.sq <= p.n_mtiles * BM;
+    if (!w.valid) {
+      w.sq = 0;
+      w.skv = 0;
+    }
+    const int64_t diag = static_cast<int64_t>(w.skv) - w.sq;
+    const int64_t o64 = diag + p.off, l64 = diag + p.left_off;
+    w.off = static_cast<int>(o64 < -w.sq - 1 ? -w.sq - 1 : (o64 > w.skv ? w.skv : o64));
+    w.left_off = static_cast<int>(l64 < -w.sq ? -w.sq : (l64 > w.skv ? w.skv : l64));
+  }
+  const int nblk_total = (w.skv + BN - 1) / BN;
+  int n_lo = 0, n_cap = nblk_total;
+  if (p.num_splits > 1) {
+    n_lo = w.split * p.blocks_per_split;
+    n_cap = min(nblk_total, n_lo + p.blocks_per_split);
+    if (n_lo > n_cap) n_lo = n_cap;
+  }
+  // The union of the tiles' ranges is contiguous: the tiles are adjacent rows.
+  int n_hi_max = n_lo, n_lo_min = n_cap;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int row0 = (w.m_cta * NQ + t) * BM;
+    int lo = n_lo, hi = n_lo;
+    if (row0 < w.sq) {
+      const int last_row = min(row0 + BM, w.sq) - 1;
+      hi = n_cap;
+      if (p.causal) hi = min(hi, floor_div(last_row + w.off, BN) + 1);
+      if (p.local) lo = max(lo, floor_div(row0 + w.left_off, BN));
+      if (hi <= lo) hi = lo = n_lo;
+    }
+    w.n_hi[t] = hi;
+    w.n_lo_t[t] = lo;
+    if (hi > lo) {
+      n_hi_max = max(n_hi_max, hi);
+      n_lo_min = min(n_lo_min, lo);
+    }
+  }
+  if (n_lo_min > n_hi_max) n_lo_min = n_hi_max;
+  w.n_hi_max = n_hi_max;
+  w.N = n_hi_max - n_lo_min;
+  return w;
+}
+
+// The j-th item of this CTA: a boustrophedon over the item list (CTA c takes c,
+// 2G - 1 - c, 2G + c, ...), so that with items in decreasing size every CTA gets
+// one large and one small item from each pair of rounds.
+__device__ __forceinline__ int item_of(int j) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return (j & 1) ? (j + 1) * G - 1 - c : j * G + c;
+}
+
 // VARLEN: packed variable-length sequences (p.cu_q / p.cu_k); a separate
 // instantiation so that the dense kernel keeps its sizes in the constant bank.
+//
+// Persistent: one CTA per SM walks its items; the producer loads the next
+// item's Q as soon as the last S MMA of the current item has read Q, and the MMA
+// warp starts the next item's S MMAs while the softmax warps write the current
+// item's output (its PV MMAs wait only until the previous O has been read out).
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
@@ -160,94 +277,31 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = q_full + NQ;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* kv_full = q_empty + 1;
   uint64_t* kv_empty = kv_full + C::STAGES;
   uint64_t* s_full = kv_empty + C::STAGES;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_full = p_full + NQ;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + NQ);
+  uint64_t* o_empty = o_full + NQ;
+  uint64_t* mma_done = o_empty + NQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   uint8_t* ring = smem + C::RING_OFF;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- which tiles this CTA owns ----
-  // Longest causal row-groups first over the whole grid (longest-processing-time
-  // order balances the SMs best; grouping CTAs by head measured slower).
-  int idx = blockIdx.x;
-  const int split = idx % p.num_splits;
-  idx /= p.num_splits;
-  const int bh = idx % (p.b * p.hq);
-  const int m_cta = p.n_mcta - 1 - idx / (p.b * p.hq);
-  const int h = bh % p.hq, bi = bh / p.hq;
-  const int kvh = h / p.g;
-
-  // ---- the sequence: one batch entry, or one packed variable-length sequence ----
-  // Packed: sequence bi owns Q rows [cu_q[bi], cu_q[bi + 1]) and K/V rows
-  // [cu_k[bi], cu_k[bi + 1]); its mask edges sit on its own bottom-right
-  // diagonal (the host passes them relative to that diagonal).
-  int sq = p.sq, skv = p.skv, off = p.off, left_off = p.left_off;
-  int q_base = 0, k_base = 0, tb = bi;  // row offsets and batch coordinate in the tensor maps
-  if constexpr (VARLEN) {
-    q_base = p.cu_q[bi];
-    sq = p.cu_q[bi + 1] - q_base;
-    k_base = p.cu_k[bi];
-    skv = p.cu_k[bi + 1] - k_base;
-    tb = 0;
-    const bool ok_seq = q_base >= 0 && sq >= 0 && q_base <= p.total_q - sq && k_base >= 0 && skv >= 0 &&
-                        k_base <= p.total_k - skv && sq <= p.n_mtiles * BM;
-    if (!ok_seq) {
-      // nothing of this CTA has started: no copy, barrier or TMEM to release
-      if (threadIdx.x == 0) record_error(p.status, kErrDeviceArg);
-      return;
-    }
-    if ((m_cta * NQ) * BM >= sq) return;  // no row of this sequence here
-    const int64_t diag = static_cast<int64_t>(skv) - sq;
-    const int64_t o64 = diag + p.off, l64 = diag + p.left_off;
-    off = static_cast<int>(o64 < -sq - 1 ? -sq - 1 : (o64 > skv ? skv : o64));
-    left_off = static_cast<int>(l64 < -sq ? -sq : (l64 > skv ? skv : l64));
-  }
-
-  const int nblk_total = (skv + BN - 1) / BN;
-  int n_lo = 0, n_cap = nblk_total;
-  if (p.num_splits > 1) {
-    n_lo = split * p.blocks_per_split;
-    n_cap = min(nblk_total, n_lo + p.blocks_per_split);
-    if (n_lo > n_cap) n_lo = n_cap;
-  }
-  // Tile t visits the blocks [n_lo_t[t], n_hi[t]) (empty when equal); the CTA
-  // streams the union [n_lo_min, n_hi_max), which is contiguous because the
-  // tiles are adjacent row ranges.
-  int n_hi[NQ], n_lo_t[NQ];
-  int n_hi_max = n_lo, n_lo_min = n_cap;
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    const int row0 = (m_cta * NQ + t) * BM;
-    int lo = n_lo, hi = n_lo;
-    if (row0 < sq) {
-      const int last_row = min(row0 + BM, sq) - 1;
-      hi = n_cap;
-      if (p.causal) hi = min(hi, floor_div(last_row + off, BN) + 1);
-      if (p.local) lo = max(lo, floor_div(row0 + left_off, BN));
-      if (hi <= lo) hi = lo = n_lo;
-    }
-    n_hi[t] = hi;
-    n_lo_t[t] = lo;
-    if (hi > lo) {
-      n_hi_max = max(n_hi_max, hi);
-      n_lo_min = min(n_lo_min, lo);
-    }
-  }
-  if (n_lo_min > n_hi_max) n_lo_min = n_hi_max;
-  const int N = n_hi_max - n_lo_min;  // KV blocks visited by the CTA
+  const int total_items = p.n_mcta * p.b * p.hq * p.num_splits;
 
   // ---- setup ----
   if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(mma_done, 1);
 #pragma unroll
     for (int t = 0; t < NQ; ++t) {
-      mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], BM);
       mbar_init(&o_full[t], 1);
+      mbar_init(&o_empty[t], BM);
     }
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) {
@@ -270,45 +324,86 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_CONTROL));
   if (warp == C::PRODUCER_WARP) {
     // =========================== TMA producer ===========================
-    if (lane == 0 && N > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
+      if (p.skv > 0 || p.total_k > 0) {  // the K/V maps exist
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+      }
       const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t gL = 0;       // K/V block loads issued by this CTA
+      uint32_t q_loads = 0;  // Q loads issued by this CTA
+      bool ok = true;
+      for (int j = 0; ok; ++j) {
+        const int item = item_of(j);
+        if (item >= total_items) break;
+        const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+        if (w.N == 0) continue;
+        // Q buffer free: the previous item's S MMAs have completed
+        if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, p.status, kSiteQEmpty)) break;
+        uint32_t q_bytes = 0;
 #pragma unroll
-      for (int t = 0; t < NQ; ++t) {
-        if (n_hi[t] > n_lo_t[t]) {
-          mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+        for (int t = 0; t < NQ; ++t)
+          if (w.n_hi[t] > w.n_lo_t[t]) q_bytes += C::Q_BYTES;
+        mbar_arrive_expect_tx(q_full, q_bytes);
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (w.n_hi[t] > w.n_lo_t[t]) {
+#pragma unroll
+            for (int c = 0; c < C::DC; ++c)
+              tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, q_full, c * 64, w.h,
+                          w.q_base + (w.m_cta * NQ + t) * BM, w.tb);
+          }
+        }
+        ++q_loads;
+        {
+          // warm L2 with the next item's Q; its load is issued only when this
+          // item's last S MMA has read the Q buffer
+          const int nxt = item_of(j + 1);
+          if (nxt < total_items) {
+            const int idx = nxt / p.num_splits;
+            const int bh = idx % (p.b * p.hq);
+            const int m_cta = p.n_mcta - 1 - idx / (p.b * p.hq);
+            const int bi = bh / p.hq, h = bh % p.hq;
+            int base = 0, rows = p.sq, tb = bi;
+            if constexpr (VARLEN) {  // (offsets are range-checked when the item itself is planned)
+              base = p.cu_q[bi];
+              rows = min(p.cu_q[bi + 1] - base, p.n_mtiles * BM);
+              tb = 0;
+            }
+#pragma unroll
+            for (int t = 0; t < NQ; ++t)
+              if ((m_cta * NQ + t) * BM < rows) {
+#pragma unroll
+                for (int c = 0; c < C::DC; ++c)
+                  tma_prefetch_l2_4d(&p.tm_q, c * 64, h, base + (m_cta * NQ + t) * BM, tb);
+              }
+          }
+        }
+        for (int L = 0; L < 2 * w.N; ++L, ++gL) {
+          const uint32_t slot = gL % C::STAGES, use = gL / C::STAGES;
+          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteKvEmpty)) {
+            ok = false;
+            break;
+          }
+          const int n = w.n_hi_max - 1 - (L >> 1);
+          const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
+          mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::DC; ++c)
-            tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, &q_full[t], c * 64, h,
-                        q_base + (m_cta * NQ + t) * BM, tb);
+            tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * 64, w.kvh,
+                             w.k_base + n * BN, w.tb, pol_kv);
         }
       }
-      int issued = 0;
-      for (int L = 0; L < 2 * N; ++L) {
-        const int slot = L % C::STAGES, use = L / C::STAGES;
-        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteKvEmpty)) break;
-        const int n = n_hi_max - 1 - (L >> 1);
-        const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
-        mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::DC; ++c)
-          tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * 64, kvh,
-                           k_base + n * BN, tb, pol_kv);
-        ++issued;
-      }
       // No copy may still be in flight when the CTA leaves: wait for the last ones.
-      for (int L = max(0, issued - C::STAGES); L < issued; ++L)
+      for (uint32_t L = gL > C::STAGES ? gL - C::STAGES : 0; L < gL; ++L)
         if (!mbar_wait(&kv_full[L % C::STAGES], (L / C::STAGES) & 1, p.status, kSiteDrain, true)) break;
-#pragma unroll
-      for (int t = 0; t < NQ; ++t)
-        if (n_hi[t] > n_lo_t[t]) mbar_wait(&q_full[t], 0, p.status, kSiteDrain, true);
+      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, p.status, kSiteDrain, true);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // =========================== MMA issuer ===========================
-    if (lane == 0 && N > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(BM, BN, BF16, false);
       constexpr uint32_t kIdO = idesc_f16(BM, D, BF16, true);
       // Descriptors are built once; per slot, tile and K step only the start
@@ -317,66 +412,97 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);  // Q tile 0, K step 0
       const uint64_t k_desc = sdesc_sw128(ring_s, 16, 1024);          // slot 0 read as K (K-major)
       const uint64_t v_desc = sdesc_sw128(ring_s, BN * 128, 1024);    // slot 0 read as V (MN-major)
-      auto active = [&](int t, int it) {
-        const int n = n_hi_max - 1 - it;
-        return n < n_hi[t] && n >= n_lo_t[t];
-      };
+      uint32_t gL = 0, q_uses = 0;
+      uint32_t pv_cnt[NQ], o_uses[NQ];
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) pv_cnt[t] = o_uses[t] = 0;
       bool ok = true;
+      for (int j = 0; ok; ++j) {
+        const int item = item_of(j);
+        if (item >= total_items) break;
+        int N, it_b[NQ], it_e[NQ];  // tile t is active in iterations [it_b[t], it_e[t])
+        {
+          const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+          N = w.N;
 #pragma unroll
-      for (int t = 0; t < NQ; ++t)
-        if (ok && n_hi[t] > n_lo_t[t]) ok = mbar_wait(&q_full[t], 0, p.status, kSiteQFull);
-      int pv_count[NQ];
-#pragma unroll
-      for (int t = 0; t < NQ; ++t) pv_count[t] = 0;
-      if (ok && (ok = mbar_wait(&kv_full[0], 0, p.status, kSiteKvFull))) {
+          for (int t = 0; t < NQ; ++t) {
+            it_b[t] = w.n_hi_max - w.n_hi[t];
+            it_e[t] = w.n_hi_max - w.n_lo_t[t];
+          }
+        }
+        if (N == 0) continue;
+#define FA_ACTIVE(t, it) ((it) >= it_b[t] && (it) < it_e[t])
+        if (!mbar_wait(q_full, q_uses & 1, p.status, kSiteQFull)) break;
+        ++q_uses;
+        if (!mbar_wait(&kv_full[gL % C::STAGES], (gL / C::STAGES) & 1, p.status, kSiteKvFull)) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
-          if (active(t, 0)) {
-            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t, 0);
+          if (FA_ACTIVE(t, 0)) {
+            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
+                                                                   gL % C::STAGES);
             umma_commit(&s_full[t]);
           }
-        umma_commit(&kv_empty[0]);
-      }
-      for (int it = 0; ok && it < N; ++it) {
-        const int Lv = 2 * it + 1, Lk = 2 * it + 2;
-        const bool has_next = it + 1 < N;
-        if (!mbar_wait(&kv_full[Lv % C::STAGES], (Lv / C::STAGES) & 1, p.status, kSiteKvFull)) break;
-        tc_fence_after();
-        bool k_ready = false;
-#pragma unroll
-        for (int t = 0; t < NQ; ++t) {
-          if (active(t, it)) {
-            // first half of P: start PV while the softmax finishes the second half
-            if (!mbar_wait(&p_full[t], pv_count[t] & 1, p.status, kSitePFull)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 16>(tbase + Cfg<D>::o_col(t),
-                                                               tbase + Cfg<D>::s_col(t), v_desc,
-                                                               Lv % C::STAGES, pv_count[t] > 0);
-            umma_commit(&o_full[t]);
-            ++pv_count[t];
+        if (N == 1) umma_commit(q_empty);  // the item's last S has been issued
+        umma_commit(&kv_empty[gL % C::STAGES]);
+        for (int it = 0; it < N; ++it) {
+          const uint32_t Lv = gL + 2 * it + 1, Lk = gL + 2 * it + 2;
+          const bool has_next = it + 1 < N;
+          if (!mbar_wait(&kv_full[Lv % C::STAGES], (Lv / C::STAGES) & 1, p.status, kSiteKvFull)) {
+            ok = false;
+            break;
           }
-          if (has_next && active(t, it + 1)) {
-            if (!k_ready) {
-              if (!mbar_wait(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) {
+          tc_fence_after();
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (FA_ACTIVE(t, it)) {
+              if (!mbar_wait(&p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
+                ok = false;
+                break;
+              }
+              // the first PV of an item overwrites O: the previous item's O must be read out
+              const bool first = it == it_b[t];
+              if (first && o_uses[t] > 0 && !mbar_wait(&o_empty[t], (o_uses[t] - 1) & 1, p.status, kSiteOEmpty)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              k_ready = true;
+              issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 16>(tbase + Cfg<D>::o_col(t),
+                                                                 tbase + Cfg<D>::s_col(t), v_desc,
+                                                                 Lv % C::STAGES, !first);
+              umma_commit(&o_full[t]);
+              ++pv_cnt[t];
             }
-            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
-                                                                   Lk % C::STAGES);
-            umma_commit(&s_full[t]);
+            if (has_next && FA_ACTIVE(t, it + 1)) {
+              if (!k_ready) {
+                if (!mbar_wait(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
+                                                                     Lk % C::STAGES);
+              umma_commit(&s_full[t]);
+            }
           }
+          if (!ok) break;
+          if (it + 2 == N) umma_commit(q_empty);  // the item's last S has been issued
+          umma_commit(&kv_empty[Lv % C::STAGES]);
+          if (has_next) umma_commit(&kv_empty[Lk % C::STAGES]);
         }
-        if (!ok) break;
-        umma_commit(&kv_empty[Lv % C::STAGES]);
-        if (has_next) umma_commit(&kv_empty[Lk % C::STAGES]);
+#pragma unroll
+        for (int t = 0; t < NQ; ++t)
+          if (it_e[t] > it_b[t]) ++o_uses[t];
+#undef FA_ACTIVE
+        gL += 2 * N;
       }
+      // Every barrier arrive of the MMAs issued above has landed before the CTA
+      // leaves (the commits complete in order).
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, p.status, kSiteDrain, true);
     }
     __syncwarp();
   }
@@ -386,224 +512,237 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = 32 * wq + lane;
-    const int row0 = (m_cta * NQ + t) * BM;
-    const int row = row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t tS = tbase + lane_off + Cfg<D>::s_col(t);
     const uint32_t tO = tbase + lane_off + Cfg<D>::o_col(t);
     const float sl2 = p.scale_log2;
-    // keys lo_row <= j < lim_row are visible to this row (the causal / window
-    // edges folded with the tail)
-    const int lim_row = p.causal ? min(skv, max(row + off + 1, 0)) : skv;
-    const int lo_row = p.local ? row + left_off : 0;
-    // (selects, not a runtime index: the arrays stay in registers)
-    const int it0 = n_hi_max - (t == 0 ? n_hi[0] : n_hi[NQ - 1]);
-    const int it_end = n_hi_max - (t == 0 ? n_lo_t[0] : n_lo_t[NQ - 1]);
-    float m_run = -INFINITY, l_run = 0.f;
-    int k = 0;
+    const bool split_mode = p.num_splits > 1;
+    uint32_t gblk = 0;  // key blocks this tile has processed, over all items
     bool ok = true;
-    for (int it = it0; it < it_end; ++it) {
-      const int n = n_hi_max - 1 - it;
-      if (!warp_wait(&s_full[t], k & 1, p.status, kSiteSFull)) {
-        ok = false;
-        break;
+    for (int j = 0; ok; ++j) {
+      const int item = item_of(j);
+      if (item >= total_items) break;
+      int row0, n_top, it0, it_end, skv, off, left_off;
+      {
+        const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+        if (VARLEN && !w.valid) {
+          if (threadIdx.x == 0) record_error(p.status, kErrDeviceArg);
+          continue;
+        }
+        row0 = (w.m_cta * NQ + t) * BM;
+        if (row0 >= w.sq) continue;  // no row of this tile in the sequence
+        n_top = w.n_hi_max - 1;
+        // (selects, not a runtime index: the arrays stay in registers)
+        it0 = w.n_hi_max - (t == 0 ? w.n_hi[0] : w.n_hi[NQ - 1]);
+        it_end = w.n_hi_max - (t == 0 ? w.n_lo_t[0] : w.n_lo_t[NQ - 1]);
+        // dense: the sizes stay constant-bank operands
+        skv = VARLEN ? w.skv : p.skv;
+        off = VARLEN ? w.off : p.off;
+        left_off = VARLEN ? w.left_off : p.left_off;
       }
-      tc_fence_after();
-      if (k > 0) {
-        // S_k complete implies PV_{k-1} complete; observe that phase of o_full so
-        // the final wait below is never more than one phase behind.
-        if (!warp_wait(&o_full[t], (k - 1) & 1, p.status, kSiteOFull)) {
+      const int row = row0 + r;
+      // keys lo_row <= j < lim_row are visible to this row (the causal / window
+      // edges folded with the tail)
+      const int lim_row = p.causal ? min(skv, max(row + off + 1, 0)) : skv;
+      const int lo_row = p.local ? row + left_off : 0;
+      float m_run = -INFINITY, l_run = 0.f;
+      int k = 0;
+      for (int it = it0; it < it_end; ++it, ++gblk, ++k) {
+        const int n = n_top - it;
+        if (!warp_wait(&s_full[t], gblk & 1, p.status, kSiteSFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      uint32_t sr[BN];
-      tmem_load_row<BN>(tS, sr);
-      float* s = reinterpret_cast<float*>(sr);
-      const bool masked = (n + 1) * BN > skv || (p.causal && (n + 1) * BN - 1 > row0 + off);
-      if (masked) {
-        const int lim = lim_row - n * BN;
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      if (p.local && n * BN < row0 + BM - 1 + left_off) {
-        const int lo = lo_row - n * BN;
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c < lo) s[c] = -INFINITY;
-      }
-      float mx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = fmax3(s[2 * i], s[2 * i + 1], s[8 + i]);
-#pragma unroll
-      for (int c = 12; c < BN; c += 8) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (c + 2 * i + 1 < BN) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        if (k > 0) {
+          // S_k complete implies PV_{k-1} complete; observe that phase of o_full so
+          // the final wait below is never more than one phase behind.
+          if (!warp_wait(&o_full[t], (gblk - 1) & 1, p.status, kSiteOFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-      }
-      const float bmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-      // The reference max moves only when the block max exceeds it by more than
-      // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
-      // unchanged); probabilities stay below 2^kRescaleLog2.
-      const float bm2 = bmax * sl2;
-      const bool grow = bm2 > m_run + kRescaleLog2;
-      const float m_new = grow ? bm2 : m_run;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
-      if (k > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_t already holds the previous blocks' product (see the o_full wait).
-        // 32 columns at a time: the 128 scores are still live in registers.
-        constexpr int CH = 32;
+        uint32_t sr[BN];
+        tmem_load_row<BN>(tS, sr);
+        float* s = reinterpret_cast<float*>(sr);
+        const bool masked = (n + 1) * BN > skv || (p.causal && (n + 1) * BN - 1 > row0 + off);
+        if (masked) {
+          const int lim = lim_row - n * BN;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += CH) {
-          uint32_t o[CH];
-          tmem_load_row<CH>(tO + c0, o);
+          for (int c = 0; c < BN; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        if (p.local && n * BN < row0 + BM - 1 + left_off) {
+          const int lo = lo_row - n * BN;
 #pragma unroll
-          for (int i = 0; i < CH; i += 2) {
-            const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
-                                        make_float2(alpha, alpha));
-            o[i] = __float_as_uint(r.x);
-            o[i + 1] = __float_as_uint(r.y);
+          for (int c = 0; c < BN; ++c)
+            if (c < lo) s[c] = -INFINITY;
+        }
+        float mx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmax3(s[2 * i], s[2 * i + 1], s[8 + i]);
+#pragma unroll
+        for (int c = 12; c < BN; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (c + 2 * i + 1 < BN) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          }
+        }
+        const float bmax = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+        // The reference max moves only when the block max exceeds it by more than
+        // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
+        // unchanged); probabilities stay below 2^kRescaleLog2.
+        const float bm2 = bmax * sl2;
+        const bool grow = bm2 > m_run + kRescaleLog2;
+        const float m_new = grow ? bm2 : m_run;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
+        if (k > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_t already holds the previous blocks' product (see the o_full wait).
+          // 32 columns at a time: the 128 scores are still live in registers.
+          constexpr int CH = 32;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += CH) {
+            uint32_t o[CH];
+            tmem_load_row<CH>(tO + c0, o);
+#pragma unroll
+            for (int i = 0; i < CH; i += 2) {
+              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                           make_float2(alpha, alpha));
+              o[i] = __float_as_uint(r2.x);
+              o[i + 1] = __float_as_uint(r2.y);
+            }
+#pragma unroll
+            for (int c = 0; c < CH; c += 32) tmem_st32(tO + c0 + c, *reinterpret_cast<const uint32_t(*)[32]>(o + c));
+          }
+        }
+        // P = 2^(s * scale * log2 e - m), written over the first half of the S
+        // columns as packed 16-bit pairs; the MMA warp is signalled once per block
+        // (a second, earlier signal for half of P measured slower).
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-m_use, -m_use);
+        float2 sum2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[BN / 4];
+#pragma unroll
+          for (int c = 0; c < BN / 2; c += 2) {
+            const int cc = half * (BN / 2) + c;
+            const float2 x = __ffma2_rn(make_float2(s[cc], s[cc + 1]), sl2v, negm);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
+            pk[c >> 1] = pack2<BF16>(e.x, e.y);
           }
 #pragma unroll
-          for (int c = 0; c < CH; c += 32) tmem_st32(tO + c0 + c, *reinterpret_cast<const uint32_t(*)[32]>(o + c));
+          for (int c = 0; c < BN / 4; c += 16)
+            tmem_st16(tS + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
+          if (half == 1) {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+          }
         }
+        const float2 s01 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+        l_run = alpha * l_run + (s01.x + s01.y);
+        m_run = m_new;
       }
-      // P = 2^(s * scale * log2 e - m), written over the first half of the S
-      // columns as packed 16-bit pairs; the MMA warp is signalled once per block
-      // (a second, earlier signal for half of P measured slower).
-      const float2 sl2v = make_float2(sl2, sl2);
-      const float2 negm = make_float2(-m_use, -m_use);
-      float2 sum2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[BN / 4];
-#pragma unroll
-        for (int c = 0; c < BN / 2; c += 2) {
-          const int cc = half * (BN / 2) + c;
-          const float2 x = __ffma2_rn(make_float2(s[cc], s[cc + 1]), sl2v, negm);
-          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
-          pk[c >> 1] = pack2<BF16>(e.x, e.y);
-        }
-#pragma unroll
-        for (int c = 0; c < BN / 4; c += 16)
-          tmem_st16(tS + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
-        if (half == 1) {
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&p_full[t]);
-        }
-      }
-      const float2 s01 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
-      l_run = alpha * l_run + (s01.x + s01.y);
-      m_run = m_new;
-      ++k;
-    }
+      if (!ok) break;
 
-    // ---------------- epilogue ----------------
-    const bool split_mode = p.num_splits > 1;
-    // LSE [b][hq][sq], or [hq][total_q] for packed sequences
-    const int64_t lse_idx = VARLEN ? static_cast<int64_t>(h) * p.total_q + q_base + row
-                                   : (static_cast<int64_t>(bi) * p.hq + h) * sq + row;
-    uint16_t* o_row = static_cast<uint16_t*>(p.o) + bi * p.o_stride_b +
-                      static_cast<int64_t>(q_base + row) * p.o_stride_row + h * p.o_stride_h;
-    if (ok && k == 0) {
-      // This tile sees no key (in this split): O = 0, LSE = -inf.
-      if (row < sq) {
-        if (split_mode) {
-          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * sq + row;
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+      // ---------------- epilogue (overlaps the next item's first MMAs) ----------------
+      const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);  // recomputed: fewer registers in the loop
+      const bool valid = row < w.sq;
+      // LSE [b][hq][sq], or [hq][total_q] for packed sequences
+      const int64_t lse_idx = VARLEN ? static_cast<int64_t>(w.h) * p.total_q + w.q_base + row
+                                     : (static_cast<int64_t>(w.bi) * p.hq + w.h) * w.sq + row;
+      const int64_t prow = ((static_cast<int64_t>(w.split) * p.b + w.bi) * p.hq + w.h) * w.sq + row;
+      if (k == 0) {
+        // This tile sees no key (in this split): O = 0, LSE = -inf.
+        if (valid) {
+          if (split_mode) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
-          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.lse[prow] = -INFINITY;
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(o_row);
+            for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse[prow] = -INFINITY;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + w.bi * p.o_stride_b +
+                                                  static_cast<int64_t>(w.q_base + row) * p.o_stride_row +
+                                                  w.h * p.o_stride_h);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[lse_idx] = -INFINITY;
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[lse_idx] = -INFINITY;
+          }
         }
+        continue;
       }
-    } else if (ok) {
-      if (warp_wait(&o_full[t], (k - 1) & 1, p.status, kSiteOFull)) {
-        tc_fence_after();
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
-        if (split_mode) {
-          // The TMEM loads are warp-collective: every lane executes them and only
-          // the global stores depend on whether the row exists.
-          const bool valid = row < sq;
-          const int64_t prow = ((static_cast<int64_t>(split) * p.b + bi) * p.hq + h) * sq + row;
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+      if (!warp_wait(&o_full[t], (gblk - 1) & 1, p.status, kSiteOFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      // O leaves TMEM 32 columns at a time (the loads are warp-collective: every
+      // lane executes them; only the global stores depend on the row existing)
+      // and goes straight to global memory; once the last columns are in
+      // registers the accumulator is released to the next item's PV MMAs.
+      if (split_mode) {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_load_row<32>(tO + c, o);
-            if (valid) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                dst[(c + i) / 4] = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
-                                               __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-            }
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_load_row<32>(tO + c, o);
+          if (c + 32 == D) {
+            tc_fence_before();
+            mbar_arrive(&o_empty[t]);
           }
-          if (valid) p.lse[prow] = lse;
-        } else if (VARLEN && row0 + BM > sq) {
-          // The last tile of a packed sequence: a 128-row TMA store would also write
-          // the next sequence's rows, so each thread stores its own row.
-          const bool valid = row < sq;
-          uint4* dst = reinterpret_cast<uint4*>(o_row);
+          if (valid) {
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_load_row<32>(tO + c, o);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (valid) {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                dst[c / 8 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            }
+            for (int i = 0; i < 32; i += 4)
+              dst[(c + i) / 4] = make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                             __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
           }
-          if (valid) p.lse[lse_idx] = lse;
-        } else {
-          // Stage O (normalised, rounded) through the Q tile's shared memory in the
-          // same 128-byte-swizzled layout the TMA store reads.
-          uint8_t* stage = smem + t * C::Q_BYTES;
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_load_row<32>(tO + c, o);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            const int cc = c >> 6;               // 64-column chunk
-            const int piece0 = (c & 63) >> 3;   // first 16-byte piece within the 128-byte row
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int piece = piece0 + q4;
-              uint4* dst = reinterpret_cast<uint4*>(stage + cc * (BM * 128) + r * 128 + ((piece ^ (r & 7)) << 4));
-              *dst = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            }
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1 + t, BM);
-          if (r == 0) {
-#pragma unroll
-            for (int cc = 0; cc < C::DC; ++cc)
-              tma_store_4d(&p.tm_o, stage + cc * (BM * 128), cc * 64, h, q_base + row0, tb);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-          }
-          if (row < sq) p.lse[lse_idx] = lse;
         }
+        if (valid) p.lse[prow] = lse;
+      } else {
+        // O leaves TMEM, normalised and rounded, HELD columns at a time (all of it
+        // for d <= 128, so that the accumulator is released at once; half for
+        // d = 256, register budget) and goes straight to global memory, each thread
+        // its own row, in 32-byte stores where the layout allows (16-byte ones
+        // otherwise).  A shared-memory staging buffer with TMA stores measured
+        // slower here: its buffer wait sits on the softmax warps' path to the next item.
+        constexpr int HELD = D <= 128 ? D : D / 2;
+        uint16_t* o_row = static_cast<uint16_t*>(p.o) + w.bi * p.o_stride_b +
+                          static_cast<int64_t>(w.q_base + row) * p.o_stride_row + w.h * p.o_stride_h;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += HELD) {
+          uint32_t pk[HELD / 2];
+#pragma unroll
+          for (int c = 0; c < HELD; c += 32) {
+            uint32_t o[32];
+            tmem_load_row<32>(tO + c0 + c, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[c / 2 + i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          }
+          if (c0 + HELD == D) {
+            tc_fence_before();
+            mbar_arrive(&o_empty[t]);  // the accumulator is free for the next item's PV MMAs
+          }
+          if (valid) {
+            if (p.o_vec32) {
+#pragma unroll
+              for (int i = 0; i < HELD / 16; ++i) st_global_v8(o_row + c0 + 16 * i, pk + 8 * i);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(o_row + c0);
+#pragma unroll
+              for (int i = 0; i < HELD / 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+        if (valid) p.lse[lse_idx] = lse;
       }
     }
   }
@@ -622,9 +761,11 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   auto kern = p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x3fffffffLL) return cudaErrorInvalidConfiguration;
+  // persistent: at most one CTA per SM, each walking its share of the items
+  const long long grid = items < p.max_ctas ? items : p.max_ctas;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
