@@ -382,7 +382,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         }
         for (int L = 0; L < 2 * w.N; ++L, ++gL) {
           const uint32_t slot = gL % C::STAGES, use = gL / C::STAGES;
-          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteKvEmpty)) {
+          // (the producer runs ahead of its consumers: it backs off while it waits)
+          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteKvEmpty, false, 128)) {
             ok = false;
             break;
           }

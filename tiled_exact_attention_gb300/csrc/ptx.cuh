@@ -80,13 +80,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // records `kErrTimeoutBase + site`) when the wait exceeds kWaitLimitNs or, unless
 // `drain` is set, when another wait of the grid has already timed out.  Waits for
 // a CTA's own copies in flight pass drain = true: those complete by themselves,
-// and the CTA must not leave before they land.
+// and the CTA must not leave before they land.  A waiter off the critical path
+// may pass sleep_ns > 0 to back off between polls, leaving issue slots to the
+// warps that share its scheduler.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int site,
-                                          bool drain = false) {
+                                          bool drain = false, uint32_t sleep_ns = 0) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0u) {
       if (!drain && error_pending(status)) return false;
