@@ -26,6 +26,9 @@ MUT_NO_ALPHA_ON_O = 1
 MUT_NO_SCALE = 2
 MUT_STRICT_CAUSAL = 4
 MUT_NO_ALPHA_ON_L = 8
+MUT_BWD_NO_D = 16
+MUT_BWD_NO_SCALE = 32
+MUT_BWD_DK_FROM_P = 64
 
 
 def build(force: bool = False) -> str:
@@ -65,6 +68,9 @@ def _load():
         lib.oracle_visible.restype = ctypes.c_int
         lib.oracle_visible_window.argtypes = [i64, i64, i64, ctypes.c_int, i64, i64, i64, ctypes.c_int]
         lib.oracle_visible_window.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64,
+                                             i64, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_split_efficiency.argtypes = [i64, i64, i64]
         lib.oracle_split_efficiency.restype = ctypes.c_double
         lib.oracle_num_splits.argtypes = [i64, i64, i64, i64]
@@ -150,6 +156,27 @@ def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = F
     if return_partials:
         return o, lse, op, lp
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, *, causal: bool = False, q_pos_offset: int | None = None,
+                  scale: float | None = None, window=(-1, -1), mutation: int = 0):
+    """Recompute-based backward pass.  Returns (dQ like q, dK like k, dV like v) for the
+    upstream gradient dout (shaped like q)."""
+    lib = _load()
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    b, sq, skv, hq, hkv, d = _shapes(q, k, v)
+    if dout.shape != q.shape:
+        raise ValueError("dout must be shaped like q")
+    off = default_offset(sq, skv) if q_pos_offset is None else int(q_pos_offset)
+    sc = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = lib.oracle_attention_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), b, sq, skv, hq, hkv, d, int(causal), off,
+                                  int(window[0]), int(window[1]), sc, _dp(dq), _dp(dk), _dp(dv), int(mutation))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd: bad arguments")
+    return dq, dk, dv
 
 
 def combine(o_part, lse_part):

@@ -30,6 +30,10 @@
  *                           carries LSE = -inf.
  *   oracle_num_splits       section 7.2 of the same page: the smallest split
  *                           count whose occupancy is at least 85% of the best.
+ *   oracle_attention_bwd    the recompute-based backward pass of "hs-black",
+ *                           sections "Backward: ..." (dV = P^T dO, dP = dO V^T,
+ *                           D = rowsum(dO * O), dS = P (dP - D), dQ = dS K * scale,
+ *                           dK = dS^T Q * scale), written out row by row.
  *
  * Sliding-window (local) attention follows "flash attention V2 code walkthrough",
  * template flag Is_local: query i sees keys in [i + skv - sq - window_left,
@@ -58,7 +62,7 @@
 #define ORACLE_MUT_STRICT_CAUSAL 4   /* both: causal j <= i + off replaced by j < ... */
 #define ORACLE_MUT_NO_ALPHA_ON_L 8   /* tiled: old denominator not rescaled by alpha */
 
-int oracle_version(void) { return 2; }
+int oracle_version(void) { return 3; }
 
 /* Visibility of key j to query row i; wl / wr < 0: that side of the window is unbounded. */
 int oracle_visible_window(int64_t i, int64_t j, int64_t skv, int causal, int64_t off, int64_t wl, int64_t wr,
@@ -316,4 +320,100 @@ int64_t oracle_num_splits(int64_t units, int64_t slots, int64_t nblk, int64_t ma
   for (int64_t s = 1; s <= smax; ++s)
     if (oracle_split_efficiency(units, slots, s) >= 0.85 * best) return s;
   return 1;
+}
+
+/*
+ * Backward pass, recompute form ("hs-black: FlashAttention 1/2/3", sections
+ * "Backward: from the softmax derivative", "Training: recompute in backward" and
+ * "Backward: back to Q, K, V").  For every row the scores are recomputed, the
+ * probabilities recovered as P = exp(S - L) with L = m + log l, and
+ *   D_i   = sum_t dO_it O_it              (one scalar per row)
+ *   dP_ij = dO_i . V_j
+ *   dS_ij = P_ij (dP_ij - D_i)            (zero where the mask hides j)
+ *   dV_j += P_ij dO_i
+ *   dQ_i += scale dS_ij K_j
+ *   dK_j += scale dS_ij Q_i
+ * with the same visibility rule as the forward pass; the query heads that share
+ * a key/value head add their contributions to its dK / dV.
+ *   q, dout: [b][sq][hq][d]; k, v: [b][skv][hkv][d]; outputs dq like q, dk / dv like k.
+ * Mutations (test only): 16 drops D, 32 drops the scale from dQ / dK, 64 uses P
+ * in place of dS for dK.  Returns 0, or -1 on bad arguments / allocation failure.
+ */
+#define ORACLE_MUT_BWD_NO_D 16
+#define ORACLE_MUT_BWD_NO_SCALE 32
+#define ORACLE_MUT_BWD_DK_FROM_P 64
+
+int oracle_attention_bwd(const double* q, const double* k, const double* v, const double* dout, int64_t b,
+                         int64_t sq, int64_t skv, int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off,
+                         int64_t wl, int64_t wr, double scale, double* dq, double* dk, double* dv, int mutation) {
+  if (hkv <= 0 || hq % hkv != 0 || d <= 0 || b < 0 || sq < 0 || skv < 0) return -1;
+  const int64_t g = hq / hkv;
+  const double gscale = (mutation & ORACLE_MUT_BWD_NO_SCALE) ? 1.0 : scale;
+  memset(dq, 0, sizeof(double) * (size_t)(b * sq * hq * d));
+  memset(dk, 0, sizeof(double) * (size_t)(b * skv * hkv * d));
+  memset(dv, 0, sizeof(double) * (size_t)(b * skv * hkv * d));
+  int bad = 0;
+  /* one (batch, key/value head) per task: its dK / dV rows are written by no other task */
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(skv > 0 ? skv : 1));
+    double* o = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !o) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t task = 0; task < b * hkv; ++task) {
+      if (!s || !o) continue;
+      const int64_t bi = task / hkv, kvh = task % hkv;
+      for (int64_t hi = kvh * g; hi < (kvh + 1) * g; ++hi) {
+        for (int64_t i = 0; i < sq; ++i) {
+          const double* qrow = q + ((bi * sq + i) * hq + hi) * d;
+          const double* dorow = dout + ((bi * sq + i) * hq + hi) * d;
+          double* dqrow = dq + ((bi * sq + i) * hq + hi) * d;
+          /* forward recomputed: scores, L = m + log l, O */
+          double m = -INFINITY;
+          int64_t nvis = 0;
+          for (int64_t j = 0; j < skv; ++j) {
+            if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, 0)) continue;
+            s[j] = scale * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
+            if (s[j] > m) m = s[j];
+            ++nvis;
+          }
+          if (nvis == 0) continue; /* no key: O = 0 and every gradient term is zero */
+          double l = 0.0;
+          for (int64_t j = 0; j < skv; ++j)
+            if (oracle_visible_window(i, j, skv, causal, off, wl, wr, 0)) l += exp(s[j] - m);
+          const double L = m + log(l);
+          for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+          for (int64_t j = 0; j < skv; ++j) {
+            if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, 0)) continue;
+            const double p = exp(s[j] - L);
+            const double* vrow = v + ((bi * skv + j) * hkv + kvh) * d;
+            for (int64_t t = 0; t < d; ++t) o[t] += p * vrow[t];
+          }
+          const double D = (mutation & ORACLE_MUT_BWD_NO_D) ? 0.0 : dot(dorow, o, d);
+          for (int64_t j = 0; j < skv; ++j) {
+            if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, 0)) continue;
+            const double p = exp(s[j] - L);
+            const double* krow = k + ((bi * skv + j) * hkv + kvh) * d;
+            const double* vrow = v + ((bi * skv + j) * hkv + kvh) * d;
+            double* dkrow = dk + ((bi * skv + j) * hkv + kvh) * d;
+            double* dvrow = dv + ((bi * skv + j) * hkv + kvh) * d;
+            const double dp = dot(dorow, vrow, d);
+            const double ds = p * (dp - D);
+            const double dk_coef = (mutation & ORACLE_MUT_BWD_DK_FROM_P) ? p : ds;
+            for (int64_t t = 0; t < d; ++t) {
+              dvrow[t] += p * dorow[t];
+              dqrow[t] += gscale * ds * krow[t];
+              dkrow[t] += gscale * dk_coef * qrow[t];
+            }
+          }
+        }
+      }
+    }
+    free(s);
+    free(o);
+  }
+  return bad ? -1 : 0;
 }
