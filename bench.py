@@ -55,7 +55,7 @@ def _dist():
 
 def _kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fa_prefill.cu", "fa_decode.cu", "ptx.cuh", "fa_internal.h"):
+    for f in ("fa_prefill.cu", "fa_decode.cu", "ptx.cuh", "fa_internal.h", "tc_common.cuh"):
         with open(os.path.join(ROOT, "tiled_exact_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -264,6 +264,48 @@ typedef struct {
  */
 fa_status fa_fwd_varlen(const fa_varlen_args* args, void* stream);
 
+/*
+ * Backward pass ("hs-black: FlashAttention 1/2/3", sections "Backward: from the
+ * softmax derivative", "Training: recompute in backward", "Backward: back to Q,
+ * K, V"): given the forward inputs, its output O and per-row LSE, and the
+ * upstream gradient dO, computes
+ *   D = rowsum(dO * O),  P = exp(S - LSE) recomputed tile by tile,
+ *   dV = P^T dO,  dS = P (dP - D) with dP = dO V^T,
+ *   dQ = dS K * scale,  dK = dS^T Q * scale,
+ * with the forward pass's mask (causal, window, tail); the query heads sharing
+ * a key/value head add their contributions to its dK and dV.  Deterministic (no
+ * atomics).  Supported: d in {64, 128}; bf16 or fp16; same layouts and stride
+ * rules as fa_fwd_args.  A caller-owned device workspace of
+ * fa_bwd_workspace_size bytes (256-byte aligned) holds D and LSE * log2(e) per
+ * row, padded to 128 rows.
+ */
+typedef struct {
+  fa_dtype dtype;
+  int32_t b, sq, skv, hq, hkv, d;
+  const void* q;        /* device, [b, sq, hq, d] */
+  const void* k;        /* device, [b, skv, hkv, d] */
+  const void* v;        /* device, [b, skv, hkv, d] */
+  const void* o;        /* device, [b, sq, hq, d]: the forward output */
+  const void* dout;     /* device, [b, sq, hq, d]: gradient of the loss with respect to O */
+  const float* lse;     /* device, fp32 [b, hq, sq]: the forward LSE */
+  void* dq;             /* device, [b, sq, hq, d], written */
+  void* dk;             /* device, [b, skv, hkv, d], written */
+  void* dv;             /* device, [b, skv, hkv, d], written */
+  int64_t q_strides[3], k_strides[3], v_strides[3], o_strides[3], do_strides[3];  /* (batch, row, head) */
+  int64_t dq_strides[3], dk_strides[3], dv_strides[3];
+  int32_t causal;       /* as fa_fwd_args */
+  int64_t q_pos_offset;
+  float scale;
+  int32_t local;
+  int64_t window_left, window_right;
+} fa_bwd_args;
+
+/* Workspace bytes fa_bwd needs (0 for invalid arguments). */
+size_t fa_bwd_workspace_size(const fa_bwd_args* args);
+
+/* Enqueue the backward pass on `stream`; FA_ERR_UNSUPPORTED for d = 256. */
+fa_status fa_bwd(const fa_bwd_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -105,6 +105,7 @@ int main(void) {
   printf("fa_fwd_args size %zu\n", sizeof(fa_fwd_args));
   printf("fa_kvcache_args size %zu\n", sizeof(fa_kvcache_args));
   printf("fa_varlen_args size %zu\n", sizeof(fa_varlen_args));
+  printf("fa_bwd_args size %zu\n", sizeof(fa_bwd_args));
   FIELDS
   return 0;
 }
@@ -114,13 +115,14 @@ int main(void) {
 def test_ctypes_mirrors_match_header_layout(tmp_path):
     """Every field of the ctypes mirrors sits at the offset, with the size, that a C
     compiler gives the structs declared in include/fa.h."""
-    from tiled_exact_attention_gb300._lib import FwdArgs, KvcacheArgs, VarlenArgs
+    from tiled_exact_attention_gb300._lib import BwdArgs, FwdArgs, KvcacheArgs, VarlenArgs
 
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
     fields = []
-    mirrors = {"fa_fwd_args": FwdArgs, "fa_kvcache_args": KvcacheArgs, "fa_varlen_args": VarlenArgs}
+    mirrors = {"fa_fwd_args": FwdArgs, "fa_kvcache_args": KvcacheArgs, "fa_varlen_args": VarlenArgs,
+               "fa_bwd_args": BwdArgs}
     for cname, py in mirrors.items():
         for name, _ in py._fields_:
             fields.append(f"F({cname}, {name})")
@@ -241,3 +243,37 @@ def test_varlen_validation_strides_and_empty(lib):
     assert lib.fa_fwd_varlen(ctypes.byref(_varlen_args(total_q=0)), None) == 0
     assert lib.fa_fwd_varlen(ctypes.byref(_varlen_args(max_seqlen_q=0)), None) == 0
     assert lib.fa_status_string(6) == b"an argument read on the device (sequence offsets) failed its check"
+
+
+def _bwd_args(**kw):
+    from tiled_exact_attention_gb300._lib import BwdArgs
+
+    a = BwdArgs()
+    a.dtype, a.b, a.sq, a.skv, a.hq, a.hkv, a.d = 0, 1, 128, 128, 2, 2, 128
+    for f in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"):
+        setattr(a, f, 4096)
+    for f in ("q_strides", "k_strides", "v_strides", "o_strides", "do_strides", "dq_strides", "dk_strides",
+              "dv_strides"):
+        setattr(a, f, (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128))
+    a.scale = 0.125
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("d", 256, 2), ("d", 96, 2), ("dout", 0, 1), ("dq", 4100, 1), ("dk", 0, 1), ("lse", 0, 1), ("hq", 3, 1),
+    ("causal", 5, 1), ("scale", -1.0, 1),
+])
+def test_bwd_validation(lib, field, value, expect):
+    a = _bwd_args(**{field: value})
+    assert lib.fa_bwd(ctypes.byref(a), None, 0, None) == expect
+    assert lib.fa_bwd_workspace_size(ctypes.byref(a)) == 0
+
+
+def test_bwd_workspace_size(lib):
+    a = _bwd_args(sq=300)
+    rows = 1 * 2 * 384  # padded to 128 rows
+    assert lib.fa_bwd_workspace_size(ctypes.byref(a)) == 2 * ((rows * 4 + 255) // 256 * 256)
+    bad = _bwd_args(dv_strides=(ctypes.c_int64 * 3)(100, 10, 1))
+    assert lib.fa_bwd(ctypes.byref(bad), None, 0, None) == 1

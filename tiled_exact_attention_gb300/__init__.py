@@ -4,6 +4,7 @@ The computation runs in libfa.so (hand-written sm_103a CUDA); this package only
 marshals torch tensors into the C ABI of include/fa.h.
 """
 from .api import (  # noqa: F401
+    fa_bwd,
     fa_fwd,
     fa_fwd_kvcache,
     fa_fwd_splitkv,

@@ -33,6 +33,8 @@ EXPORTS = (
     "fa_kvcache_workspace_size",
     "fa_fwd_kvcache",
     "fa_fwd_varlen",
+    "fa_bwd_workspace_size",
+    "fa_bwd",
     "fa_splitkv_combine",
     "fa_sync_status",
     "fa_selftest_wait_timeout",
@@ -132,6 +134,43 @@ class VarlenArgs(ctypes.Structure):
     ]
 
 
+class BwdArgs(ctypes.Structure):
+    """Mirror of `fa_bwd_args`."""
+
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("b", ctypes.c_int32),
+        ("sq", ctypes.c_int32),
+        ("skv", ctypes.c_int32),
+        ("hq", ctypes.c_int32),
+        ("hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("dout", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p),
+        ("dk", ctypes.c_void_p),
+        ("dv", ctypes.c_void_p),
+        ("q_strides", ctypes.c_int64 * 3),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3),
+        ("o_strides", ctypes.c_int64 * 3),
+        ("do_strides", ctypes.c_int64 * 3),
+        ("dq_strides", ctypes.c_int64 * 3),
+        ("dk_strides", ctypes.c_int64 * 3),
+        ("dv_strides", ctypes.c_int64 * 3),
+        ("causal", ctypes.c_int32),
+        ("q_pos_offset", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+        ("local", ctypes.c_int32),
+        ("window_left", ctypes.c_int64),
+        ("window_right", ctypes.c_int64),
+    ]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -174,6 +213,10 @@ def load():
         lib.fa_fwd_kvcache.restype = ctypes.c_int
         lib.fa_fwd_varlen.argtypes = [ctypes.POINTER(VarlenArgs), vp]
         lib.fa_fwd_varlen.restype = ctypes.c_int
+        lib.fa_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdArgs)]
+        lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.fa_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp, ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

@@ -13,7 +13,7 @@ import math
 import torch
 
 from . import _lib
-from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, FwdArgs, KvcacheArgs, VarlenArgs, check
+from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, BwdArgs, FwdArgs, KvcacheArgs, VarlenArgs, check
 
 _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
@@ -268,6 +268,51 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int | No
                          scale=scale, window=window)
     check(_lib.load().fa_fwd_varlen(ctypes.byref(a), _stream_handle(stream)), "fa_fwd_varlen")
     return out, lse
+
+
+def make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, *, causal: bool, scale: float | None,
+                  q_pos_offset: int | None, window=None) -> BwdArgs:
+    """Fill `fa_bwd_args` from [b, s, h, d] tensors (lse fp32 [b, hq, sq])."""
+    _check_qkv(q, k, v)
+    for name, t, like in (("o", o, q), ("dout", dout, q), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.shape != like.shape or t.dtype != q.dtype \
+                or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a CUDA tensor shaped and typed like its forward counterpart")
+    b, sq, hq, d = q.shape
+    if lse.shape != (b, hq, sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [b, hq, sq]")
+    a = BwdArgs()
+    a.dtype = _DT[q.dtype]
+    a.b, a.sq, a.skv, a.hq, a.hkv, a.d = b, sq, k.shape[1], hq, k.shape[2], d
+    a.q, a.k, a.v, a.o, a.dout, a.lse = (t.data_ptr() for t in (q, k, v, o, dout, lse))
+    a.dq, a.dk, a.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    a.q_strides, a.k_strides, a.v_strides = _strides(q), _strides(k), _strides(v)
+    a.o_strides, a.do_strides = _strides(o), _strides(dout)
+    a.dq_strides, a.dk_strides, a.dv_strides = _strides(dq), _strides(dk), _strides(dv)
+    a.causal = 1 if causal else 0
+    a.q_pos_offset = FA_OFFSET_BOTTOM_RIGHT if q_pos_offset is None else int(q_pos_offset)
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    if window is not None:
+        a.local = 1
+        a.window_left, a.window_right = int(window[0]), int(window[1])
+    return a
+
+
+def fa_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
+           q_pos_offset: int | None = None, window=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass for the forward call with the same arguments; returns (dQ, dK, dV)."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    a = make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, scale=scale, q_pos_offset=q_pos_offset,
+                      window=window)
+    lib = _lib.load()
+    if workspace is None:
+        need = int(lib.fa_bwd_workspace_size(ctypes.byref(a)))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    check(lib.fa_bwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                     workspace.numel() * workspace.element_size(), _stream_handle(stream)), "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_splitkv_combine(o_part, lse_part, out, lse=None, stream=None):

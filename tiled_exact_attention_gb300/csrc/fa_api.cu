@@ -683,6 +683,130 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   return from_cuda(launch_prefill(p, a->d, a->dtype, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// The forward description of a backward problem (validation and the mask plan are shared).
+fa_fwd_args fwd_view(const fa_bwd_args* a) {
+  fa_fwd_args f;
+  std::memset(&f, 0, sizeof(f));
+  f.dtype = a->dtype;
+  f.b = a->b;
+  f.sq = a->sq;
+  f.skv = a->skv;
+  f.hq = a->hq;
+  f.hkv = a->hkv;
+  f.d = a->d;
+  f.q = a->q;
+  f.k = a->k;
+  f.v = a->v;
+  f.o = const_cast<void*>(a->o);
+  f.lse = const_cast<float*>(a->lse);
+  for (int i = 0; i < 3; ++i) {
+    f.q_strides[i] = a->q_strides[i];
+    f.k_strides[i] = a->k_strides[i];
+    f.v_strides[i] = a->v_strides[i];
+    f.o_strides[i] = a->o_strides[i];
+  }
+  f.causal = a->causal;
+  f.q_pos_offset = a->q_pos_offset;
+  f.scale = a->scale;
+  f.local = a->local;
+  f.window_left = a->window_left;
+  f.window_right = a->window_right;
+  return f;
+}
+
+fa_status validate_bwd(const fa_bwd_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  const fa_fwd_args f = fwd_view(a);
+  const fa_status v = validate(&f);
+  if (v != FA_OK) return v;
+  if (!bwd_supported(a->d)) return FA_ERR_UNSUPPORTED;
+  if (a->sq == 0 && a->skv == 0) return FA_OK;
+  if (a->sq > 0) {
+    if (a->dout == nullptr || a->dq == nullptr || !aligned(a->dout, 16) || !aligned(a->dq, 16))
+      return FA_ERR_INVALID_ARG;
+    if (!strides_ok(a->do_strides) || !strides_ok(a->dq_strides)) return FA_ERR_INVALID_ARG;
+  }
+  if (a->skv > 0) {
+    if (a->dk == nullptr || a->dv == nullptr || !aligned(a->dk, 16) || !aligned(a->dv, 16))
+      return FA_ERR_INVALID_ARG;
+    if (!strides_ok(a->dk_strides) || !strides_ok(a->dv_strides)) return FA_ERR_INVALID_ARG;
+    if (a->sq == 0 && (a->k == nullptr || a->v == nullptr)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+size_t bwd_workspace_bytes(const fa_bwd_args* a) {
+  const size_t rows = static_cast<size_t>(a->b) * a->hq * static_cast<size_t>(ceil_div64(a->sq, 128) * 128);
+  return 2 * align256(rows * sizeof(float));
+}
+
+}  // namespace
+
+size_t fa_bwd_workspace_size(const fa_bwd_args* a) {
+  if (validate_bwd(a) != FA_OK) return 0;
+  const size_t w = bwd_workspace_bytes(a);
+  return w > 0 ? w : 256;
+}
+
+fa_status fa_bwd(const fa_bwd_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  const fa_status v = validate_bwd(a);
+  if (v != FA_OK) return v;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a->sq == 0 && a->skv == 0) return FA_OK;  // (sq == 0 alone: the dK / dV kernel writes zeros)
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  const size_t need = bwd_workspace_bytes(a);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return FA_ERR_INVALID_ARG;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const fa_fwd_args f = fwd_view(a);
+  if (a->sq > 0 &&
+      (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hq, a->sq, a->b, a->q_strides, 64, 128, true) ||
+       !encode_map(&p.tm_do, a->dout, a->dtype, a->d, a->hq, a->sq, a->b, a->do_strides, 64, 128, true)))
+    return FA_ERR_INVALID_ARG;
+  if (a->skv > 0 &&
+      (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, 128, true) ||
+       !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, 128, true)))
+    return FA_ERR_INVALID_ARG;
+  const MaskPlan c = plan_mask(&f);
+  p.o = a->o;
+  p.dout = a->dout;
+  p.lse = a->lse;
+  p.dq = a->dq;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  for (int i = 0; i < 3; ++i) {
+    p.o_st[i] = a->o_strides[i];
+    p.do_st[i] = a->do_strides[i];
+    p.dq_st[i] = a->dq_strides[i];
+    p.dk_st[i] = a->dk_strides[i];
+    p.dv_st[i] = a->dv_strides[i];
+  }
+  p.b = a->b;
+  p.sq = a->sq;
+  p.skv = a->skv;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
+  p.n_ntiles = static_cast<int>(ceil_div64(a->skv, 128));
+  p.sq_pad = p.n_mtiles * 128;
+  p.causal = c.causal;
+  p.off = c.off;
+  p.local = c.local;
+  p.left_off = c.left_off;
+  p.scale = a->scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  const size_t rows = static_cast<size_t>(a->b) * a->hq * p.sq_pad;
+  p.dpre = static_cast<float*>(workspace);
+  p.l2pre = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * sizeof(float)));
+  p.status = di.status;
+  return from_cuda(launch_bwd(p, a->d, a->dtype, st));
+}
+
 fa_status fa_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   DeviceInfo di;

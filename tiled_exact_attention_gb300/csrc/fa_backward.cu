@@ -1,0 +1,586 @@
+// Backward pass in the recompute form of "hs-black: FlashAttention 1/2/3",
+// sections "Backward: from the softmax derivative", "Training: recompute in
+// backward" and "Backward: back to Q, K, V": the forward pass keeps only O and
+// one L = m + log l per row; the backward pass recomputes S tile by tile,
+// recovers P = exp(S - L), and forms
+//   D = rowsum(dO * O), dP = dO V^T, dS = P (dP - D),
+//   dV = P^T dO, dQ = dS K * scale, dK = dS^T Q * scale,
+// with P and dS zero where the mask hides a key.  Three kernels:
+//   * fa_bwd_pre_kernel: D and L * log2(e) per row (HBM-bound, one warp per row);
+//   * fa_bwd_dq_kernel: a CTA owns 128 query rows and streams the key blocks
+//     they see (S = Q K^T, dP = dO V^T, dQ += dS K on tcgen05, one TMEM lane per
+//     row for the elementwise work);
+//   * fa_bwd_dkdv_kernel: a CTA owns 128 keys of one key/value head and streams
+//     the query tiles that see them, over every query head of its group (S^T =
+//     K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q, one TMEM lane per key),
+//     so dK and dV are reduced in TMEM without atomics.
+// Splitting dQ from dK / dV costs two extra products per block pair (S and dP
+// are computed by both kernels) but needs no atomic accumulation and keeps every
+// accumulator of a CTA in its 512 TMEM columns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Wait sites of the backward kernels (recorded in the status word on timeout).
+enum : int {
+  kSiteBwdQFull = 32,
+  kSiteBwdKvFull,
+  kSiteBwdKvEmpty,
+  kSiteBwdSFull,
+  kSiteBwdDsFull,
+  kSiteBwdDone,
+  kSiteBwdDrain,
+  kSiteBwdQdFull,
+  kSiteBwdQdEmpty,
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;             // query rows per tile
+  static constexpr int BN = 128;             // keys per block
+  static constexpr int DC = D / 64;          // 64-column chunks (128-byte rows)
+  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int THREADS = 256;        // 4 elementwise warps + producer + MMA + 2 idle
+  static constexpr int PRODUCER_WARP = 4;
+  static constexpr int MMA_WARP = 5;
+  static constexpr int TMEM_COLS = 512;
+  // dQ kernel: Q and dO tiles, then a ring of K / V blocks
+  static constexpr int DQ_STAGES = 4;
+  static constexpr int DQ_RING_OFF = 2 * TILE_BYTES;
+  static constexpr int DQ_BAR_OFF = DQ_RING_OFF + DQ_STAGES * TILE_BYTES;
+  // (at least 117 KiB, so that one CTA, which holds all 512 TMEM columns, runs per SM)
+  static constexpr int MIN_SMEM = 117 * 1024;
+  static constexpr int DQ_SMEM_RAW = DQ_BAR_OFF + 8 * (1 + 2 * DQ_STAGES + 3) + 16 + 1024;
+  static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
+  // dK / dV kernel: K and V tiles, then stages of (Q tile, dO tile, L and D of their rows)
+  static constexpr int KV_STAGES = 2;
+  static constexpr int QD_STAGE_BYTES = 2 * TILE_BYTES + 1024;  // + 128 floats of L, 128 of D
+  static constexpr int QD_OFF = 2 * TILE_BYTES;
+  static constexpr int KV_BAR_OFF = QD_OFF + KV_STAGES * QD_STAGE_BYTES;
+  static constexpr int KV_SMEM_RAW = KV_BAR_OFF + 8 * (1 + 2 * KV_STAGES + 3) + 16 + 1024;
+  static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
+  static_assert(DQ_SMEM <= 227 * 1024 && KV_SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(QD_STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  // TMEM: S (or S^T) at 0, dP (or dP^T) at 128, accumulators from 256
+  static constexpr int S_COL = 0, DP_COL = 128, ACC_COL = 256;
+  static_assert(ACC_COL + 2 * D <= TMEM_COLS, "dK and dV accumulators must fit in TMEM");
+};
+
+// ------------------------------------------------------------------ preprocess
+
+// One warp per (batch, head, padded row): D = sum_t dO_t O_t in fp32 from the
+// stored (rounded) O, and L2 = LSE * log2(e); padding rows and rows that see no
+// key get L2 = +inf, so that every probability recovered from it is 0.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int EPL = D / 32;  // elements per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nrows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp; row < nrows;
+       row += static_cast<int64_t>(gridDim.x) * 8) {
+    const int i = static_cast<int>(row % p.sq_pad);
+    const int64_t bh = row / p.sq_pad;
+    const int h = static_cast<int>(bh % p.hq), bi = static_cast<int>(bh / p.hq);
+    float dsum = 0.f, l2 = INFINITY;
+    if (i < p.sq) {
+      const uint16_t* orow = static_cast<const uint16_t*>(p.o) + bi * p.o_st[0] + static_cast<int64_t>(i) * p.o_st[1] +
+                             h * p.o_st[2] + lane * EPL;
+      const uint16_t* drow = static_cast<const uint16_t*>(p.dout) + bi * p.do_st[0] +
+                             static_cast<int64_t>(i) * p.do_st[1] + h * p.do_st[2] + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const uint32_t ou = *reinterpret_cast<const uint32_t*>(orow + e);
+        const uint32_t du = *reinterpret_cast<const uint32_t*>(drow + e);
+        float o0, o1, d0, d1;
+        if constexpr (BF16) {
+          o0 = __uint_as_float(ou << 16);
+          o1 = __uint_as_float(ou & 0xffff0000u);
+          d0 = __uint_as_float(du << 16);
+          d1 = __uint_as_float(du & 0xffff0000u);
+        } else {
+          const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ou));
+          const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&du));
+          o0 = of.x;
+          o1 = of.y;
+          d0 = df.x;
+          d1 = df.y;
+        }
+        dsum = fmaf(o0, d0, dsum);
+        dsum = fmaf(o1, d1, dsum);
+      }
+#pragma unroll
+      for (int x = 16; x > 0; x >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, x);
+      const float lse = p.lse[(static_cast<int64_t>(bi) * p.hq + h) * p.sq + i];
+      l2 = lse > -INFINITY ? lse * kLog2e : INFINITY;
+    }
+    if (lane == 0) {
+      p.dpre[row] = dsum;
+      p.l2pre[row] = l2;
+    }
+  }
+}
+
+// Store one row of D fp32 values (scaled by `mul`) from TMEM columns [col, col + D)
+// of this thread's lane to global memory as 16-bit values (when `valid`).
+template <int D, bool BF16>
+__device__ __forceinline__ void store_acc_row(uint32_t tcol, float mul, uint16_t* dst, bool valid) {
+#pragma unroll
+  for (int c = 0; c < D; c += 32) {
+    uint32_t v[32];
+    tmem_load_row<32>(tcol + c, v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+
+// Key blocks [lo, hi) that some row of the 128-row tile starting at row0 sees.
+__device__ __forceinline__ void key_block_range(const BwdParams& p, int row0, int* lo, int* hi) {
+  const int nblk = (p.skv + 127) / 128;
+  const int last_row = min(row0 + 128, p.sq) - 1;
+  int h = nblk, l = 0;
+  if (p.causal) h = min(h, floor_div(last_row + p.off, 128) + 1);
+  if (p.local) l = max(l, floor_div(row0 + p.left_off, 128));
+  if (h < l) h = l;
+  *lo = l;
+  *hi = h;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, ST = C::DQ_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem + C::DQ_RING_OFF;
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::DQ_BAR_OFF);  // Q and dO landed
+  uint64_t* kv_full = q_full + 1;
+  uint64_t* kv_empty = kv_full + ST;
+  uint64_t* s_full = kv_empty + ST;   // S and dP of a block are in TMEM
+  uint64_t* ds_full = s_full + 1;     // dS of a block is in TMEM (count 128)
+  uint64_t* dq_done = ds_full + 1;    // every dQ MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // longest row tiles first (causal: the last tiles see the most keys)
+  const int bh = blockIdx.x % (p.b * p.hq);
+  const int m = p.n_mtiles - 1 - static_cast<int>(blockIdx.x / (p.b * p.hq));
+  const int h = bh % p.hq, bi = bh / p.hq, kvh = h / p.g;
+  const int row0 = m * BM;
+  int n_lo, n_hi;
+  key_block_range(p, row0, &n_lo, &n_hi);
+  const int N = n_hi - n_lo;  // key blocks visited, from n_hi - 1 down
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, BM);
+    mbar_init(dq_done, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == C::PRODUCER_WARP) {
+    if (lane == 0 && N > 0) {
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem + c * (BM * 128), &p.tm_q, q_full, c * 64, h, row0, bi);
+        tma_load_4d(smem + C::TILE_BYTES + c * (BM * 128), &p.tm_do, q_full, c * 64, h, row0, bi);
+      }
+      const uint64_t pol = l2_policy_evict_last();
+      int issued = 0;
+      for (int L = 0; L < 2 * N; ++L) {
+        const int slot = L % ST, use = L / ST;
+        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteBwdKvEmpty, false, 128)) break;
+        const int n = n_hi - 1 - (L >> 1);
+        mbar_arrive_expect_tx(&kv_full[slot], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_4d_hint(ring + slot * C::TILE_BYTES + c * (BN * 128), (L & 1) ? &p.tm_v : &p.tm_k,
+                           &kv_full[slot], c * 64, kvh, n * BN, bi, pol);
+        ++issued;
+      }
+      for (int L = max(0, issued - ST); L < issued; ++L)
+        if (!mbar_wait(&kv_full[L % ST], (L / ST) & 1, p.status, kSiteBwdDrain, true)) break;
+      mbar_wait(q_full, 0, p.status, kSiteBwdDrain, true);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0 && N > 0) {
+      constexpr uint32_t kIdS = idesc_f16(BM, BN, BF16, false);
+      constexpr uint32_t kIdQ = idesc_f16(BM, D, BF16, true);
+      const uint32_t ring_s = smem_u32(ring);
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::TILE_BYTES), 16, 1024);
+      const uint64_t kk_desc = sdesc_sw128(ring_s, 16, 1024);        // a ring slot read K-major
+      const uint64_t kmn_desc = sdesc_sw128(ring_s, BN * 128, 1024);  // a ring slot read MN-major
+      bool ok = mbar_wait(q_full, 0, p.status, kSiteBwdQFull);
+      for (int it = 0; ok && it < N; ++it) {
+        const int Lk = 2 * it, Lv = 2 * it + 1;
+        if (!mbar_wait(&kv_full[Lk % ST], (Lk / ST) & 1, p.status, kSiteBwdKvFull) ||
+            !mbar_wait(&kv_full[Lv % ST], (Lv / ST) & 1, p.status, kSiteBwdKvFull))
+          break;
+        tc_fence_after();
+        // S = Q K^T and dP = dO V^T (the previous dQ MMA has read the dS columns: in order)
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, q_desc, kk_desc, 0, Lk % ST);
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0,
+                                                                    Lv % ST);
+        umma_commit(s_full);
+        umma_commit(&kv_empty[Lv % ST]);
+        if (!mbar_wait(ds_full, it & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
+        // dQ += dS K: dS from TMEM (over the S columns), K read MN-major
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, BN / 16>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc,
+                                                              Lk % ST, it > 0);
+        umma_commit(&kv_empty[Lk % ST]);
+      }
+      umma_commit(dq_done);
+      mbar_wait(dq_done, 0, p.status, kSiteBwdDrain, true);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------- elementwise: one query row per thread ----------------
+    const int r = 32 * warp + lane;
+    const int row = row0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t tS = tbase + lane_off + C::S_COL;
+    const uint32_t tP = tbase + lane_off + C::DP_COL;
+    const int64_t prow = (static_cast<int64_t>(bi) * p.hq + h) * p.sq_pad + row;  // row < sq_pad
+    const float l2 = p.l2pre[prow];
+    const float dd = p.dpre[prow];
+    const float sl2 = p.scale_log2;
+    // keys lo_row <= j < lim_row are visible to this row
+    const int lim_row = p.causal ? min(p.skv, max(row + p.off + 1, 0)) : p.skv;
+    const int lo_row = p.local ? row + p.left_off : 0;
+    bool ok = true;
+    for (int it = 0; it < N; ++it) {
+      const int n = n_hi - 1 - it;
+      if (!warp_wait(s_full, it & 1, p.status, kSiteBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int lim = lim_row - n * BN, lo = lo_row - n * BN;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t sv[32], pv[32];
+        tmem_load_row<32>(tS + c0, sv);
+        tmem_load_row<32>(tP + c0, pv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = c0 + i + e;
+            const bool vis = c < lim && c >= lo;
+            const float pr = vis ? ex2_approx(__uint_as_float(sv[i + e]) * sl2 - l2) : 0.f;
+            ds[e] = pr * (__uint_as_float(pv[i + e]) - dd);
+          }
+          pk[i / 2] = pack2<BF16>(ds[0], ds[1]);
+        }
+        tmem_st16(tS + c0 / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    uint16_t* dst = static_cast<uint16_t*>(p.dq) + bi * p.dq_st[0] + static_cast<int64_t>(row) * p.dq_st[1] +
+                    h * p.dq_st[2];
+    if (ok && N > 0 && warp_wait(dq_done, 0, p.status, kSiteBwdDone)) {
+      tc_fence_after();
+      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL, p.scale, dst, row < p.sq);
+    } else if (ok && N == 0 && row < p.sq) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+
+// Query tiles [lo, hi) with some row that sees a key of the block starting at key j0.
+__device__ __forceinline__ void query_tile_range(const BwdParams& p, int j0, int* lo, int* hi) {
+  const int j_last = min(j0 + 127, p.skv - 1);
+  int l = 0, h = p.n_mtiles;
+  if (p.causal) l = max(l, floor_div(j0 - p.off, 128));       // row i sees j0 only if i >= j0 - off
+  if (p.local) h = min(h, floor_div(j_last - p.left_off, 128) + 1);  // ... j_last only if i <= j_last - left_off
+  if (h < l) h = l;
+  *lo = l;
+  *hi = h;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BM = C::BM, BN = C::BN, ST = C::KV_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::KV_BAR_OFF);  // K and V landed
+  uint64_t* qd_full = kv_full + 1;   // per stage: Q, dO, L2, D of a query tile landed
+  uint64_t* qd_empty = qd_full + ST;
+  uint64_t* s_full = qd_empty + ST;  // S^T and dP^T in TMEM
+  uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (count 128)
+  uint64_t* mma_done = p_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  auto stage_ptr = [&](int s) { return smem + C::QD_OFF + s * C::QD_STAGE_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = blockIdx.x % p.n_ntiles;
+  const int bk = blockIdx.x / p.n_ntiles;
+  const int kvh = bk % p.hkv, bi = bk / p.hkv;
+  const int j0 = nb * BN;
+  int m_lo, m_hi;
+  query_tile_range(p, j0, &m_lo, &m_hi);
+  const int nm = m_hi - m_lo;
+  const int T = nm * p.g;  // query tiles visited: every head of the group, rows m_lo.. of each
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, BM);
+    mbar_init(mma_done, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&qd_full[s], 1);
+      mbar_init(&qd_empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == C::PRODUCER_WARP) {
+    if (lane == 0 && T > 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem + c * (BN * 128), &p.tm_k, kv_full, c * 64, kvh, j0, bi);
+        tma_load_4d(smem + C::TILE_BYTES + c * (BN * 128), &p.tm_v, kv_full, c * 64, kvh, j0, bi);
+      }
+      int issued = 0;
+      for (int ti = 0; ti < T; ++ti) {
+        const int s = ti % ST, use = ti / ST;
+        if (use > 0 && !mbar_wait(&qd_empty[s], (use - 1) & 1, p.status, kSiteBwdQdEmpty, false, 128)) break;
+        const int h = kvh * p.g + ti / nm, m = m_lo + ti % nm;
+        uint8_t* st = stage_ptr(s);
+        mbar_arrive_expect_tx(&qd_full[s], 2 * C::TILE_BYTES + 1024);
+#pragma unroll
+        for (int c = 0; c < C::DC; ++c) {
+          tma_load_4d(st + c * (BM * 128), &p.tm_q, &qd_full[s], c * 64, h, m * BM, bi);
+          tma_load_4d(st + C::TILE_BYTES + c * (BM * 128), &p.tm_do, &qd_full[s], c * 64, h, m * BM, bi);
+        }
+        const int64_t prow = (static_cast<int64_t>(bi) * p.hq + h) * p.sq_pad + m * BM;
+        bulk_load(st + 2 * C::TILE_BYTES, p.l2pre + prow, 512, &qd_full[s]);
+        bulk_load(st + 2 * C::TILE_BYTES + 512, p.dpre + prow, 512, &qd_full[s]);
+        ++issued;
+      }
+      for (int ti = max(0, issued - ST); ti < issued; ++ti)
+        if (!mbar_wait(&qd_full[ti % ST], (ti / ST) & 1, p.status, kSiteBwdDrain, true)) break;
+      mbar_wait(kv_full, 0, p.status, kSiteBwdDrain, true);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t kIdS = idesc_f16(BN, BM, BF16, false);  // S^T: M = keys, N = query rows
+      constexpr uint32_t kIdA = idesc_f16(BN, D, BF16, true);    // dV, dK: M = keys, N = d, B MN-major
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::TILE_BYTES), 16, 1024);
+      bool ok = mbar_wait(kv_full, 0, p.status, kSiteBwdKvFull);
+      for (int ti = 0; ok && ti < T; ++ti) {
+        const int s = ti % ST;
+        if (!mbar_wait(&qd_full[s], (ti / ST) & 1, p.status, kSiteBwdQdFull)) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(stage_ptr(s));
+        const uint64_t qk_desc = sdesc_sw128(st, 16, 1024);                            // Q, K-major
+        const uint64_t dok_desc = sdesc_sw128(st + C::TILE_BYTES, 16, 1024);          // dO, K-major
+        const uint64_t qmn_desc = sdesc_sw128(st, BM * 128, 1024);                     // Q, MN-major
+        const uint64_t domn_desc = sdesc_sw128(st + C::TILE_BYTES, BM * 128, 1024);  // dO, MN-major
+        // S^T = K Q^T, dP^T = V dO^T (the previous dV / dK MMAs have read these columns: in order)
+        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, k_desc, qk_desc, 0, 0);
+        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, v_desc, dok_desc, 0, 0);
+        umma_commit(s_full);
+        if (!mbar_wait(p_full, ti & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q (P^T, dS^T from TMEM; dO, Q read MN-major)
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 16>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0,
+                                                              ti > 0);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 16>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
+                                                              ti > 0);
+        umma_commit(&qd_empty[s]);
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, p.status, kSiteBwdDrain, true);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------- elementwise: one key per thread, query rows along the columns ----------------
+    const int r = 32 * warp + lane;
+    const int j = j0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t tS = tbase + lane_off + C::S_COL;
+    const uint32_t tP = tbase + lane_off + C::DP_COL;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int ti = 0; ti < T; ++ti) {
+      const int s = ti % ST;
+      const int m = m_lo + ti % nm;
+      // the L2 and D vectors were written by the copy engine: observe their arrival
+      if (!warp_wait(&qd_full[s], (ti / ST) & 1, p.status, kSiteBwdQdFull) ||
+          !warp_wait(s_full, ti & 1, p.status, kSiteBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* l2v = reinterpret_cast<const float*>(stage_ptr(s) + 2 * C::TILE_BYTES);
+      const float* dv = l2v + 128;
+      // row i (column c) sees this key iff c >= cmin and c <= cmax (relative to the tile)
+      const int i0 = m * BM;
+      int cmin = 0, cmax = BM - 1;
+      if (j >= p.skv) cmin = BM;  // a key past the end: nothing
+      if (p.causal) cmin = max(cmin, j - p.off - i0);        // j <= i + off
+      if (p.local) cmax = min(cmax, j - p.left_off - i0);    // j >= i + left_off
+#pragma unroll
+      for (int c0 = 0; c0 < BM; c0 += 32) {
+        uint32_t sv[32], pv[32];
+        tmem_load_row<32>(tS + c0, sv);
+        tmem_load_row<32>(tP + c0, pv);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = c0 + i + e;
+            const bool vis = c >= cmin && c <= cmax;
+            pr[e] = vis ? ex2_approx(__uint_as_float(sv[i + e]) * sl2 - l2v[c]) : 0.f;
+            ds[e] = pr[e] * (__uint_as_float(pv[i + e]) - dv[c]);
+          }
+          pp[i / 2] = pack2<BF16>(pr[0], pr[1]);
+          pd[i / 2] = pack2<BF16>(ds[0], ds[1]);
+        }
+        tmem_st16(tS + c0 / 2, pp);
+        tmem_st16(tP + c0 / 2, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    const bool valid = j < p.skv;
+    uint16_t* dvr = static_cast<uint16_t*>(p.dv) + bi * p.dv_st[0] + static_cast<int64_t>(j) * p.dv_st[1] +
+                    kvh * p.dv_st[2];
+    uint16_t* dkr = static_cast<uint16_t*>(p.dk) + bi * p.dk_st[0] + static_cast<int64_t>(j) * p.dk_st[1] +
+                    kvh * p.dk_st[2];
+    if (ok && T > 0 && warp_wait(mma_done, 0, p.status, kSiteBwdDone)) {
+      tc_fence_after();
+      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL, 1.f, dvr, valid);
+      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL + D, p.scale, dkr, valid);
+    } else if (ok && T == 0 && valid) {
+      // no query row sees these keys: zero gradients
+      uint4* a = reinterpret_cast<uint4*>(dvr);
+      uint4* b = reinterpret_cast<uint4*>(dkr);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) a[c] = b[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  {
+    const int64_t rows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
+    const int64_t blocks = (rows + 7) / 8;
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
+    if (grid > 0) fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = fa_bwd_dq_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DQ_SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = static_cast<int64_t>(p.n_mtiles) * p.b * p.hq;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (grid > 0) kern<<<static_cast<unsigned>(grid), C::THREADS, C::DQ_SMEM, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = fa_bwd_dkdv_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = static_cast<int64_t>(p.n_ntiles) * p.b * p.hkv;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (grid > 0) kern<<<static_cast<unsigned>(grid), C::THREADS, C::KV_SMEM, stream>>>(p);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+bool bwd_supported(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_bwd(const BwdParams& p, int d, int dtype, cudaStream_t stream) {
+  const bool bf16 = dtype == 0;
+  switch (d) {
+    case 64:
+      return bf16 ? launch_bwd_t<64, true>(p, stream) : launch_bwd_t<64, false>(p, stream);
+    case 128:
+      return bf16 ? launch_bwd_t<128, true>(p, stream) : launch_bwd_t<128, false>(p, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

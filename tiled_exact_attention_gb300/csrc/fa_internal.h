@@ -70,6 +70,31 @@ struct DecodeParams {
   const int* cu_seqlens;        // packed: [b + 1] prefix sums of keys per sequence
 };
 
+// Parameters of the backward kernels (recompute form: D and log2-scaled LSE per
+// row are prepared once, then dQ and dK / dV are computed by two kernels).
+struct BwdParams {
+  CUtensorMap tm_q;   // Q  [b][sq][hq][d],   box {64, 1, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_do;  // dO like Q
+  CUtensorMap tm_k;   // K  [b][skv][hkv][d], box {64, 1, 128, 1}
+  CUtensorMap tm_v;   // V  like K
+  const void* o;      // O (forward output), strides o_st (b, row, head) in elements
+  const void* dout;   // dO, strides do_st
+  const float* lse;   // [b][hq][sq]
+  int64_t o_st[3], do_st[3];
+  void* dq;           // outputs, strides (b, row, head) in elements
+  void* dk;
+  void* dv;
+  int64_t dq_st[3], dk_st[3], dv_st[3];
+  float* dpre;        // D  = rowsum(dO * O), [b][hq][sq_pad]; 0 on padding rows
+  float* l2pre;       // LSE * log2(e), [b][hq][sq_pad]; +inf on padding rows and rows that see no key
+  int b, sq, skv, hq, hkv, g, sq_pad;
+  int causal, off;    // row i sees key j only if j <= i + off (when causal)
+  int local, left_off;  // ... and only if j >= i + left_off (when local)
+  float scale, scale_log2;
+  int n_mtiles, n_ntiles;  // 128-row query tiles, 128-key blocks
+  int* status;
+};
+
 struct CombineParams {
   const float* o_part;   // [ns][b][hq][sq][d]
   const float* lse_part; // [ns][b][hq][sq]
@@ -93,5 +118,9 @@ bool decode_supported(int d, int g);
 cudaError_t launch_combine(const CombineParams& p, int dtype, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
+
+// Backward: preprocess, dQ and dK / dV kernels in sequence on `stream`.
+cudaError_t launch_bwd(const BwdParams& p, int d, int dtype, cudaStream_t stream);
+bool bwd_supported(int d);
 
 }  // namespace fa
