@@ -260,6 +260,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
+    bwd = bench_backward(dev, flush, steps=max(10, min(100, K // 50)))
 
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
     kv_bytes = 2 * wd.b * wd.hkv * wd.skv * wd.d * 2
@@ -321,6 +322,9 @@ def run_ours(args):
         "decode_paged": dict(paged, roofline={"bound": "hbm", "achieved": paged["value"], "peak": hbm,
                                               "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
                                               "peak_source": peak_src, "traffic": None}),
+        "backward": dict(bwd, roofline={"bound": "tensor", "achieved": bwd["value"], "peak": pk, "unit": "TFLOP/s",
+                                        "frac": round(bwd["value"] / pk, 4), "peak_source": f"{peak_src} sustained",
+                                        "frac_of_burst": round(bwd["value"] / pk_burst, 4), "traffic": None}),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
                      "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
                      "kernel": "fa_prefill_kernel<128, bf16>",
@@ -339,6 +343,49 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def bench_backward(dev, flush, steps=30, warmup=3):
+    """Backward pass (fa_bwd) on the causal-prefill workload with a seeded upstream gradient; TFLOP/s by the
+    usual 2.5x-forward accounting (five products of 2*d flops per visible pair)."""
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_bwd, fa_fwd, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import BASE_SEED, WORKLOADS, make_qkv, normal
+
+    w = WORKLOADS["causal_prefill"]
+    q, k, v = (t.to(dev) for t in make_qkv(w))
+    do = normal(tuple(q.shape), BASE_SEED + w.index, 7, 1.0, q.dtype).to(dev)
+    o, lse = fa_fwd(q, k, v, causal=True, q_pos_offset=w.offset)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        fa_bwd(q, k, v, o, lse, do, causal=True, q_pos_offset=w.offset, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if fa_sync_status() != 0:
+        raise RuntimeError("device status set by the backward pass")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    pairs = w.visible_pairs_per_head() * w.b * w.hq
+    flops = 2.5 * 4.0 * w.d * pairs
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "causal": True},
+            "flops_per_launch": flops, "flops_executed_per_launch": 3.5 * 4.0 * w.d * pairs,
+            "accounting": "2.5x the forward flops (dV, dP, dQ, dK and the recomputed S); the kernels execute 3.5x "
+                          "(S and dP are recomputed by both the dQ and the dK/dV kernel)",
+            "kernels": "fa_bwd_pre_kernel + fa_bwd_dq_kernel + fa_bwd_dkdv_kernel", "steps": steps}
 
 
 def bench_paged_decode(dev, flush, steps=200, warmup=5):
