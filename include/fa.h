@@ -306,6 +306,68 @@ size_t fa_bwd_workspace_size(const fa_bwd_args* args);
 /* Enqueue the backward pass on `stream`; FA_ERR_UNSUPPORTED for d = 256. */
 fa_status fa_bwd(const fa_bwd_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * 8-bit forward path ("hs-black: FlashAttention 1/2/3", section "FlashAttention-3:
+ * precision and hardware": FP8 as an extra speed path, a scale factor per block,
+ * the scales carried into the computation, softmax statistics kept in fp32).
+ *
+ * fa_quantize_e4m3 turns one bf16 / fp16 tensor [b, s, h, d] (d in {64, 128})
+ * into e4m3 codes: descale = amax / 448 over each 128-row block of one (batch,
+ * head) (per_head = 0; descale [b, h, ceil(s / 128)]) or over the whole (batch,
+ * head) (per_head = 1; descale [b, h]); code = round-to-nearest-even e4m3 of
+ * x * (1 / descale), saturating at +-448 (fp32 IEEE products, so the codes are
+ * reproducible bit for bit).  An all-zero block gets descale 1.  Output
+ * row-major [b, s, h, d] with out_strides (batch, row, head) in bytes, or
+ * (transpose = 1) [b, h, d, s] with out_strides (batch, head, d-row) in bytes,
+ * the row index contiguous; strides multiples of 16 bytes, base 16-byte aligned.
+ */
+typedef struct {
+  fa_dtype dtype;              /* input storage type */
+  int32_t b, s, h, d;
+  const void* x;               /* device, [b, s, h, d] */
+  int64_t x_strides[3];        /* (batch, row, head) in elements, multiples of 8 */
+  void* out;                   /* device, e4m3 codes */
+  int64_t out_strides[3];
+  int32_t transpose;           /* 0 or 1 */
+  int32_t per_head;            /* 0 or 1 */
+  float* descale;              /* device, written */
+} fa_quant_args;
+
+fa_status fa_quantize_e4m3(const fa_quant_args* args, void* stream);
+
+/*
+ * Forward pass with e4m3 Q, K, V (d = 128): S = (Q8 K8^T) * q_descale[tile of
+ * 128 rows] * k_descale[block of 128 keys] * scale, P = exp(S - m) rounded to e4m3
+ * for the P V product (P <= 2^8 by the lazy-rescale rule, within e4m3's range),
+ * row max and sum in fp32, O = (P8 V8) * v_descale[head] / l written as bf16,
+ * LSE fp32.  Q, K as produced by fa_quantize_e4m3 with per-block scales; V
+ * transposed ([b, hkv, d, skv]) with one scale per (batch, head), applied to the
+ * whole accumulator since a per-block V scale folded into P could push P past 448.
+ * Same mask, GQA and offset rules as fa_fwd; no split-KV or packed sequences.
+ */
+typedef struct {
+  int32_t b, sq, skv, hq, hkv, d;
+  const void* q;               /* device, e4m3 [b, sq, hq, d] */
+  const void* k;               /* device, e4m3 [b, skv, hkv, d] */
+  const void* vt;              /* device, e4m3 [b, hkv, d, skv] */
+  const float* q_descale;      /* device, [b, hq, ceil(sq / 128)] */
+  const float* k_descale;      /* device, [b, hkv, ceil(skv / 128)] */
+  const float* v_descale;      /* device, [b, hkv] */
+  void* o;                     /* device, bf16 [b, sq, hq, d], written */
+  float* lse;                  /* device, fp32 [b, hq, sq], written */
+  int64_t q_strides[3];        /* (batch, row, head) in bytes */
+  int64_t k_strides[3];
+  int64_t vt_strides[3];       /* (batch, head, d-row) in bytes */
+  int64_t o_strides[3];        /* (batch, row, head) in elements */
+  int32_t causal;
+  int64_t q_pos_offset;
+  float scale;
+  int32_t local;
+  int64_t window_left, window_right;
+} fa_fwd_e4m3_args;
+
+fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* args, void* stream);
+
 /* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -106,6 +106,8 @@ int main(void) {
   printf("fa_kvcache_args size %zu\n", sizeof(fa_kvcache_args));
   printf("fa_varlen_args size %zu\n", sizeof(fa_varlen_args));
   printf("fa_bwd_args size %zu\n", sizeof(fa_bwd_args));
+  printf("fa_quant_args size %zu\n", sizeof(fa_quant_args));
+  printf("fa_fwd_e4m3_args size %zu\n", sizeof(fa_fwd_e4m3_args));
   FIELDS
   return 0;
 }
@@ -115,14 +117,14 @@ int main(void) {
 def test_ctypes_mirrors_match_header_layout(tmp_path):
     """Every field of the ctypes mirrors sits at the offset, with the size, that a C
     compiler gives the structs declared in include/fa.h."""
-    from tiled_exact_attention_gb300._lib import BwdArgs, FwdArgs, KvcacheArgs, VarlenArgs
+    from tiled_exact_attention_gb300._lib import BwdArgs, E4m3Args, FwdArgs, KvcacheArgs, QuantArgs, VarlenArgs
 
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
     fields = []
     mirrors = {"fa_fwd_args": FwdArgs, "fa_kvcache_args": KvcacheArgs, "fa_varlen_args": VarlenArgs,
-               "fa_bwd_args": BwdArgs}
+               "fa_bwd_args": BwdArgs, "fa_quant_args": QuantArgs, "fa_fwd_e4m3_args": E4m3Args}
     for cname, py in mirrors.items():
         for name, _ in py._fields_:
             fields.append(f"F({cname}, {name})")
@@ -277,3 +279,34 @@ def test_bwd_workspace_size(lib):
     assert lib.fa_bwd_workspace_size(ctypes.byref(a)) == 2 * ((rows * 4 + 255) // 256 * 256)
     bad = _bwd_args(dv_strides=(ctypes.c_int64 * 3)(100, 10, 1))
     assert lib.fa_bwd(ctypes.byref(bad), None, 0, None) == 1
+
+
+def test_e4m3_validation(lib):
+    from tiled_exact_attention_gb300._lib import E4m3Args, QuantArgs
+
+    qa = QuantArgs()
+    qa.dtype, qa.b, qa.s, qa.h, qa.d = 0, 1, 256, 2, 128
+    qa.x = qa.out = qa.descale = 4096
+    qa.x_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+    qa.out_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+    for field, value, expect in (("d", 256, 2), ("d", 96, 2), ("transpose", 2, 1), ("x", 0, 1), ("out", 4104, 1)):
+        old = getattr(qa, field)
+        setattr(qa, field, value)
+        assert lib.fa_quantize_e4m3(ctypes.byref(qa), None) == expect, field
+        setattr(qa, field, old)
+    qa.out_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 8)  # not a multiple of 16 bytes
+    assert lib.fa_quantize_e4m3(ctypes.byref(qa), None) == 1
+    a = E4m3Args()
+    a.b, a.sq, a.skv, a.hq, a.hkv, a.d = 1, 128, 128, 2, 2, 128
+    for f in ("q", "k", "vt", "q_descale", "k_descale", "v_descale", "o", "lse"):
+        setattr(a, f, 4096)
+    for f in ("q_strides", "k_strides", "vt_strides"):
+        setattr(a, f, (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128))
+    a.o_strides = (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128)
+    a.scale = 0.1
+    for field, value, expect in (("d", 64, 2), ("d", 256, 2), ("vt", 0, 1), ("v_descale", 0, 1), ("causal", 3, 1),
+                                 ("scale", 0.0, 1), ("hq", 3, 1)):
+        old = getattr(a, field)
+        setattr(a, field, value)
+        assert lib.fa_fwd_e4m3(ctypes.byref(a), None) == expect, field
+        setattr(a, field, old)

@@ -8,9 +8,12 @@ from .api import (  # noqa: F401
     fa_fwd,
     fa_fwd_kvcache,
     fa_fwd_splitkv,
+    fa_fwd_e4m3,
     fa_fwd_splitkv_noalloc,
     fa_fwd_varlen,
     fa_num_splits_heuristic,
+    fa_quantize_e4m3,
+    quantize_qkv_e4m3,
     fa_selftest_wait_timeout,
     fa_splitkv_combine,
     fa_splitkv_default_splits,

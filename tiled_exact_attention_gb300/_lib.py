@@ -35,6 +35,8 @@ EXPORTS = (
     "fa_fwd_varlen",
     "fa_bwd_workspace_size",
     "fa_bwd",
+    "fa_quantize_e4m3",
+    "fa_fwd_e4m3",
     "fa_splitkv_combine",
     "fa_sync_status",
     "fa_selftest_wait_timeout",
@@ -171,6 +173,56 @@ class BwdArgs(ctypes.Structure):
     ]
 
 
+class QuantArgs(ctypes.Structure):
+    """Mirror of `fa_quant_args`."""
+
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("b", ctypes.c_int32),
+        ("s", ctypes.c_int32),
+        ("h", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("x", ctypes.c_void_p),
+        ("x_strides", ctypes.c_int64 * 3),
+        ("out", ctypes.c_void_p),
+        ("out_strides", ctypes.c_int64 * 3),
+        ("transpose", ctypes.c_int32),
+        ("per_head", ctypes.c_int32),
+        ("descale", ctypes.c_void_p),
+    ]
+
+
+class E4m3Args(ctypes.Structure):
+    """Mirror of `fa_fwd_e4m3_args`."""
+
+    _fields_ = [
+        ("b", ctypes.c_int32),
+        ("sq", ctypes.c_int32),
+        ("skv", ctypes.c_int32),
+        ("hq", ctypes.c_int32),
+        ("hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("vt", ctypes.c_void_p),
+        ("q_descale", ctypes.c_void_p),
+        ("k_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("q_strides", ctypes.c_int64 * 3),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("vt_strides", ctypes.c_int64 * 3),
+        ("o_strides", ctypes.c_int64 * 3),
+        ("causal", ctypes.c_int32),
+        ("q_pos_offset", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+        ("local", ctypes.c_int32),
+        ("window_left", ctypes.c_int64),
+        ("window_right", ctypes.c_int64),
+    ]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -217,6 +269,10 @@ def load():
         lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
         lib.fa_bwd.argtypes = [ctypes.POINTER(BwdArgs), vp, ctypes.c_size_t, vp]
         lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_quantize_e4m3.argtypes = [ctypes.POINTER(QuantArgs), vp]
+        lib.fa_quantize_e4m3.restype = ctypes.c_int
+        lib.fa_fwd_e4m3.argtypes = [ctypes.POINTER(E4m3Args), vp]
+        lib.fa_fwd_e4m3.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

@@ -13,7 +13,8 @@ import math
 import torch
 
 from . import _lib
-from ._lib import FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, BwdArgs, FwdArgs, KvcacheArgs, VarlenArgs, check
+from ._lib import (FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, BwdArgs, E4m3Args, FwdArgs, KvcacheArgs, QuantArgs,
+                   VarlenArgs, check)
 
 _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
@@ -313,6 +314,75 @@ def fa_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None =
     check(lib.fa_bwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                      workspace.numel() * workspace.element_size(), _stream_handle(stream)), "fa_bwd")
     return dq, dk, dv
+
+
+def fa_quantize_e4m3(x, *, per_head: bool = False, transpose: bool = False, stream=None):
+    """e4m3 codes (torch.uint8) of a [b, s, h, d] bf16/fp16 tensor and their descales (fp32).
+    Codes are [b, s, h, d], or [b, h, d, s_pad] (s_pad = s rounded up to 16) with transpose=True;
+    descales are [b, h, ceil(s / 128)] per 128-row block, or [b, h] with per_head=True."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype not in _DT or x.dim() != 4 or x.stride(3) != 1:
+        raise ValueError("x must be a CUDA bf16/fp16 [b, s, h, d] tensor with contiguous d")
+    b, s, h, d = x.shape
+    if transpose:
+        sp = (s + 15) // 16 * 16
+        out = torch.zeros((b, h, d, sp), dtype=torch.uint8, device=x.device)
+        ost = (out.stride(0), out.stride(1), out.stride(2))
+    else:
+        out = torch.empty((b, s, h, d), dtype=torch.uint8, device=x.device)
+        ost = (out.stride(0), out.stride(1), out.stride(2))
+    ds = torch.empty((b, h) if per_head else (b, h, (s + 127) // 128), dtype=torch.float32, device=x.device)
+    a = QuantArgs()
+    a.dtype = _DT[x.dtype]
+    a.b, a.s, a.h, a.d = b, s, h, d
+    a.x = x.data_ptr()
+    a.x_strides = _strides(x)
+    a.out = out.data_ptr()
+    a.out_strides = (ctypes.c_int64 * 3)(*ost)
+    a.transpose, a.per_head = int(bool(transpose)), int(bool(per_head))
+    a.descale = ds.data_ptr()
+    check(_lib.load().fa_quantize_e4m3(ctypes.byref(a), _stream_handle(stream)), "fa_quantize_e4m3")
+    return out, ds
+
+
+def quantize_qkv_e4m3(q, k, v, stream=None):
+    """The inputs fa_fwd_e4m3 expects: (q8, q_descale), (k8, k_descale) per 128-row block, and V
+    transposed with one descale per (batch, head)."""
+    return (fa_quantize_e4m3(q, stream=stream), fa_quantize_e4m3(k, stream=stream),
+            fa_quantize_e4m3(v, per_head=True, transpose=True, stream=stream))
+
+
+def fa_fwd_e4m3(q8, q_descale, k8, k_descale, vt8, v_descale, *, causal: bool = False, scale: float | None = None,
+                q_pos_offset: int | None = None, window=None, out=None, lse=None, stream=None):
+    """Forward pass on e4m3 inputs (see fa_quantize_e4m3); returns (O bf16 [b, sq, hq, d], LSE [b, hq, sq])."""
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 \
+                or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a CUDA uint8 4-D tensor with a contiguous last dimension")
+    b, sq, hq, d = q8.shape
+    skv, hkv = k8.shape[1], k8.shape[2]
+    if k8.shape != (b, skv, hkv, d) or vt8.shape[:3] != (b, hkv, d) or vt8.shape[3] < skv:
+        raise ValueError("inconsistent q8 / k8 / vt8 shapes")
+    if out is None:
+        out = torch.empty((b, sq, hq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((b, hq, sq), dtype=torch.float32, device=q8.device)
+    a = E4m3Args()
+    a.b, a.sq, a.skv, a.hq, a.hkv, a.d = b, sq, skv, hq, hkv, d
+    a.q, a.k, a.vt = q8.data_ptr(), k8.data_ptr(), vt8.data_ptr()
+    a.q_descale, a.k_descale, a.v_descale = q_descale.data_ptr(), k_descale.data_ptr(), v_descale.data_ptr()
+    a.o, a.lse = out.data_ptr(), lse.data_ptr()
+    a.q_strides = (ctypes.c_int64 * 3)(q8.stride(0), q8.stride(1), q8.stride(2))
+    a.k_strides = (ctypes.c_int64 * 3)(k8.stride(0), k8.stride(1), k8.stride(2))
+    a.vt_strides = (ctypes.c_int64 * 3)(vt8.stride(0), vt8.stride(1), vt8.stride(2))
+    a.o_strides = _strides(out)
+    a.causal = 1 if causal else 0
+    a.q_pos_offset = FA_OFFSET_BOTTOM_RIGHT if q_pos_offset is None else int(q_pos_offset)
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    if window is not None:
+        a.local = 1
+        a.window_left, a.window_right = int(window[0]), int(window[1])
+    check(_lib.load().fa_fwd_e4m3(ctypes.byref(a), _stream_handle(stream)), "fa_fwd_e4m3")
+    return out, lse
 
 
 def fa_splitkv_combine(o_part, lse_part, out, lse=None, stream=None):

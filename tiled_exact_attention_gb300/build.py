@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_backward.cu"]
+SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_backward.cu", "fa_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -122,6 +122,24 @@ bool encode_map(CUtensorMap* m, const void* ptr, fa_dtype dt, int d, int h, int 
   return r == CUDA_SUCCESS;
 }
 
+// General 4-D map over one-byte elements: dims innermost first, strides in bytes
+// of dims 1..3, the given box, 128-byte swizzle.
+bool encode_map_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], const int64_t strides_b[3],
+                   const uint32_t box_in[4]) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4];
+  for (int i = 0; i < 4; ++i) dims[i] = static_cast<cuuint64_t>(dims_in[i] > 0 ? dims_in[i] : 1);
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(strides_b[0]), static_cast<cuuint64_t>(strides_b[1]),
+                           static_cast<cuuint64_t>(strides_b[2])};
+  cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // The mask as the kernels use it: row i sees key j < skv only if
@@ -805,6 +823,146 @@ fa_status fa_bwd(const fa_bwd_args* a, void* workspace, size_t workspace_bytes, 
   p.l2pre = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * sizeof(float)));
   p.status = di.status;
   return from_cuda(launch_bwd(p, a->d, a->dtype, st));
+}
+
+namespace {
+
+bool strides16_ok(const int64_t s[3]) {
+  for (int i = 0; i < 3; ++i) {
+    if (s[i] <= 0 || (s[i] % 16) != 0) return false;
+    if (s[i] >= (static_cast<int64_t>(1) << 40)) return false;
+  }
+  return true;
+}
+
+fa_status validate_quant(const fa_quant_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->s < 0 || a->h < 1) return FA_ERR_INVALID_ARG;
+  if ((a->transpose != 0 && a->transpose != 1) || (a->per_head != 0 && a->per_head != 1)) return FA_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128) return FA_ERR_UNSUPPORTED;
+  if (a->s > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (a->s == 0) return FA_OK;
+  if (a->x == nullptr || a->out == nullptr || a->descale == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a->x, 16) || !aligned(a->out, 16) || !aligned(a->descale, 4)) return FA_ERR_INVALID_ARG;
+  if (!strides_ok(a->x_strides) || !strides16_ok(a->out_strides)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status validate_e4m3(const fa_fwd_e4m3_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->sq < 0 || a->skv < 0 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0)
+    return FA_ERR_INVALID_ARG;
+  if ((a->causal != 0 && a->causal != 1) || (a->local != 0 && a->local != 1)) return FA_ERR_INVALID_ARG;
+  if (a->local && (a->window_left < -1 || a->window_right < -1)) return FA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (!prefill_e4m3_supported(a->d)) return FA_ERR_UNSUPPORTED;
+  if (a->sq > (1 << 30) || a->skv > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (a->sq == 0) return FA_OK;
+  if (a->q == nullptr || a->o == nullptr || a->lse == nullptr || a->q_descale == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4) || !aligned(a->q_descale, 4))
+    return FA_ERR_INVALID_ARG;
+  if (!strides16_ok(a->q_strides) || !strides_ok(a->o_strides)) return FA_ERR_INVALID_ARG;
+  if (a->skv > 0) {
+    if (a->k == nullptr || a->vt == nullptr || a->k_descale == nullptr || a->v_descale == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(a->k, 16) || !aligned(a->vt, 16) || !aligned(a->k_descale, 4) || !aligned(a->v_descale, 4))
+      return FA_ERR_INVALID_ARG;
+    if (!strides16_ok(a->k_strides) || !strides16_ok(a->vt_strides)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+}  // namespace
+
+fa_status fa_quantize_e4m3(const fa_quant_args* a, void* stream) {
+  const fa_status v = validate_quant(a);
+  if (v != FA_OK || a->s == 0) return v;
+  QuantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.x = a->x;
+  p.out = a->out;
+  p.descale = a->descale;
+  for (int i = 0; i < 3; ++i) {
+    p.x_st[i] = a->x_strides[i];
+    p.out_st[i] = a->out_strides[i];
+  }
+  p.b = a->b;
+  p.s = a->s;
+  p.h = a->h;
+  p.d = a->d;
+  p.nblk = static_cast<int>(ceil_div64(a->s, 128));
+  p.transpose = a->transpose;
+  p.per_head = a->per_head;
+  return from_cuda(launch_quant_e4m3(p, a->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* a, void* stream) {
+  const fa_status v = validate_e4m3(a);
+  if (v != FA_OK || a->sq == 0) return v;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const uint64_t qd[4] = {static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hq), static_cast<uint64_t>(a->sq),
+                            static_cast<uint64_t>(a->b)};
+    const int64_t qs[3] = {a->q_strides[2], a->q_strides[1], a->q_strides[0]};
+    const uint32_t box[4] = {static_cast<uint32_t>(a->d), 1, 128, 1};  // one 128-row tile, 128 bytes per row
+    if (!encode_map_u8(&p.tm_q, a->q, qd, qs, box)) return FA_ERR_INVALID_ARG;
+  }
+  if (a->skv > 0) {
+    const uint64_t kd[4] = {static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hkv), static_cast<uint64_t>(a->skv),
+                            static_cast<uint64_t>(a->b)};
+    const int64_t ks[3] = {a->k_strides[2], a->k_strides[1], a->k_strides[0]};
+    // V transposed: dims (key, d-row, head, batch)
+    const uint64_t vd[4] = {static_cast<uint64_t>(a->skv), static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hkv),
+                            static_cast<uint64_t>(a->b)};
+    const int64_t vs[3] = {a->vt_strides[2], a->vt_strides[1], a->vt_strides[0]};
+    const uint32_t kbox[4] = {static_cast<uint32_t>(a->d), 1, 128, 1};
+    const uint32_t vbox[4] = {128, static_cast<uint32_t>(a->d), 1, 1};  // 128 keys of every d-row
+    if (!encode_map_u8(&p.tm_k, a->k, kd, ks, kbox) || !encode_map_u8(&p.tm_v, a->vt, vd, vs, vbox))
+      return FA_ERR_INVALID_ARG;
+  }
+  fa_fwd_args f;
+  std::memset(&f, 0, sizeof(f));
+  f.sq = a->sq;
+  f.skv = a->skv;
+  f.causal = a->causal;
+  f.q_pos_offset = a->q_pos_offset;
+  f.local = a->local;
+  f.window_left = a->window_left;
+  f.window_right = a->window_right;
+  const MaskPlan c = plan_mask(&f);
+  p.o = a->o;
+  p.lse = a->lse;
+  p.o_stride_b = a->o_strides[0];
+  p.o_stride_row = a->o_strides[1];
+  p.o_stride_h = a->o_strides[2];
+  p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0 &&
+              a->o_strides[2] % 16 == 0;
+  p.b = a->b;
+  p.sq = a->sq;
+  p.skv = a->skv;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.causal = c.causal;
+  p.off = c.off;
+  p.local = c.local;
+  p.left_off = c.left_off;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
+  p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+  p.num_splits = 1;
+  p.blocks_per_split = static_cast<int>(ceil_div64(a->skv, 128));
+  p.max_ctas = di.sms;
+  p.status = di.status;
+  p.q_descale = a->q_descale;
+  p.k_descale = a->k_descale;
+  p.v_descale = a->v_descale;
+  p.n_kblocks = static_cast<int>(ceil_div64(a->skv, 128));
+  return from_cuda(launch_prefill_e4m3(p, a->d, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_sync_status(void* stream) {

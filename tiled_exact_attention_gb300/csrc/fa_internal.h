@@ -36,6 +36,13 @@ struct PrefillParams {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // e4m3 inputs (null descales otherwise): S = (Q8 K8^T) * q_descale[tile] *
+  // k_descale[block] * scale, O = (P8 V8) * v_descale[head] / l; tm_v then maps
+  // V transposed, [b][hkv][d][skv] with the key index innermost.
+  const float* q_descale;  // [b][hq][n_mtiles]
+  const float* k_descale;  // [b][hkv][n_kblocks]
+  const float* v_descale;  // [b][hkv]
+  int n_kblocks;
 };
 
 // Where the decode kernel finds a sequence's keys.
@@ -95,6 +102,17 @@ struct BwdParams {
   int* status;
 };
 
+// e4m3 quantisation of one [b][s][h][d] tensor.
+struct QuantParams {
+  const void* x;      // bf16 / fp16, strides x_st (b, row, head) in elements
+  int64_t x_st[3];
+  void* out;          // e4m3; row-major: out_st = (b, row, head) bytes; transposed: (b, head, d-row) bytes
+  int64_t out_st[3];
+  float* descale;     // [b][h][nblk] (per 128-row block) or [b][h] (per head)
+  int b, s, h, d, nblk;
+  int transpose, per_head;
+};
+
 struct CombineParams {
   const float* o_part;   // [ns][b][hq][sq][d]
   const float* lse_part; // [ns][b][hq][sq]
@@ -106,6 +124,9 @@ struct CombineParams {
 
 // Launchers: return cudaSuccess or the launch error.  `dtype` 0 = bf16, 1 = fp16.
 cudaError_t launch_prefill(const PrefillParams& p, int d, int dtype, cudaStream_t stream);
+cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stream);  // bf16 output
+bool prefill_e4m3_supported(int d);
+cudaError_t launch_quant_e4m3(const QuantParams& p, int dtype, cudaStream_t stream);
 int prefill_block_n(int d);   // keys per KV block of the prefill kernel
 int prefill_q_tiles(int d);   // 128-row Q tiles per CTA
 

@@ -33,15 +33,18 @@ namespace {
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 
-template <int D>
+// E8: e4m3 Q, K, V (one byte per element) and e4m3 P.
+template <int D, bool E8 = false>
 struct Cfg {
+  static constexpr int ELT = E8 ? 1 : 2;             // bytes per input element
   static constexpr int BM = 128;                     // rows per Q tile (= TMEM lanes)
   static constexpr int NQ = (D <= 128) ? 2 : 1;      // Q tiles per CTA
   static constexpr int BN = (D <= 128) ? 128 : 64;   // keys per K/V block
-  static constexpr int STAGES = (D == 64) ? 8 : 4;   // K/V ring slots
-  static constexpr int DC = D / 64;                  // 64-column (128-byte) chunks
-  static constexpr int Q_BYTES = BM * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int STAGES = (E8 || D == 64) ? 8 : 4;  // K/V ring slots
+  static constexpr int DC = D * ELT / 128;           // 128-byte chunks per row
+  static constexpr int CHUNK_ELEMS = 128 / ELT;      // elements per chunk
+  static constexpr int Q_BYTES = BM * D * ELT;
+  static constexpr int KV_BYTES = BN * D * ELT;
   // softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle
   // warps) so that register budgets can be moved between whole warpgroups
   static constexpr int NUM_WARPS = 4 * NQ + 4;
@@ -170,6 +173,23 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   return w;
 }
 
+// The S and PV products in the 16-bit or the e4m3 form.
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool E8>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int t, int slot) {
+  if constexpr (E8)
+    issue_s_tile_e4m3<D, BN, BM, Q_BYTES, KV_BYTES, ID>(d_tmem, q_desc, k_desc, t, slot);
+  else
+    issue_s_tile<D, BN, BM, Q_BYTES, KV_BYTES, ID>(d_tmem, q_desc, k_desc, t, slot);
+}
+
+template <int D, int BN, int KV_BYTES, uint32_t ID, bool E8>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, int slot, bool acc) {
+  if constexpr (E8)
+    issue_pv_tile_e4m3<D, BN, KV_BYTES, ID>(o_tmem, p_tmem, v_desc, slot, acc);
+  else
+    issue_pv_tile<D, BN, KV_BYTES, ID, 0, BN / 16>(o_tmem, p_tmem, v_desc, slot, acc);
+}
+
 // The j-th item of this CTA: a boustrophedon over the item list (CTA c takes c,
 // 2G - 1 - c, 2G + c, ...), so that with items in decreasing size every CTA gets
 // one large and one small item from each pair of rounds.
@@ -185,9 +205,9 @@ __device__ __forceinline__ int item_of(int j) {
 // item's Q as soon as the last S MMA of the current item has read Q, and the MMA
 // warp starts the next item's S MMAs while the softmax warps write the current
 // item's output (its PV MMAs wait only until the previous O has been read out).
-template <int D, bool BF16, bool VARLEN>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using C = Cfg<D>;
+template <int D, bool BF16, bool VARLEN, bool E8 = false>
+__global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using C = Cfg<D, E8>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -268,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
           if (w.n_hi[t] > w.n_lo_t[t]) {
 #pragma unroll
             for (int c = 0; c < C::DC; ++c)
-              tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, q_full, c * 64, w.h,
+              tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, q_full, c * C::CHUNK_ELEMS, w.h,
                           w.q_base + (w.m_cta * NQ + t) * BM, w.tb);
           }
         }
@@ -293,7 +313,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
               if ((m_cta * NQ + t) * BM < rows) {
 #pragma unroll
                 for (int c = 0; c < C::DC; ++c)
-                  tma_prefetch_l2_4d(&p.tm_q, c * 64, h, base + (m_cta * NQ + t) * BM, tb);
+                  tma_prefetch_l2_4d(&p.tm_q, c * C::CHUNK_ELEMS, h, base + (m_cta * NQ + t) * BM, tb);
               }
           }
         }
@@ -305,12 +325,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
             break;
           }
           const int n = w.n_hi_max - 1 - (L >> 1);
-          const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
           mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
+          if (E8 && (L & 1)) {
+            // V transposed ([d rows][keys]): one box of D rows x BN keys
+            tma_load_4d_hint(ring + slot * C::KV_BYTES, &p.tm_v, &kv_full[slot], w.k_base + n * BN, 0, w.kvh, w.tb,
+                             pol_kv);
+          } else {
+            const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
 #pragma unroll
-          for (int c = 0; c < C::DC; ++c)
-            tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * 64, w.kvh,
-                             w.k_base + n * BN, w.tb, pol_kv);
+            for (int c = 0; c < C::DC; ++c)
+              tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * C::CHUNK_ELEMS,
+                               w.kvh, w.k_base + n * BN, w.tb, pol_kv);
+          }
         }
       }
       // No copy may still be in flight when the CTA leaves: wait for the last ones.
@@ -322,14 +348,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
   } else if (warp == C::MMA_WARP) {
     // =========================== MMA issuer ===========================
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(BM, BN, BF16, false);
-      constexpr uint32_t kIdO = idesc_f16(BM, D, BF16, true);
+      constexpr uint32_t kIdS = E8 ? idesc_e4m3(BM, BN) : idesc_f16(BM, BN, BF16, false);
+      constexpr uint32_t kIdO = E8 ? idesc_e4m3(BM, D) : idesc_f16(BM, D, BF16, true);
       // Descriptors are built once; per slot, tile and K step only the start
       // address field (low bits, address >> 4) moves, by compile-time amounts.
       const uint32_t ring_s = smem_u32(ring);
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);  // Q tile 0, K step 0
       const uint64_t k_desc = sdesc_sw128(ring_s, 16, 1024);          // slot 0 read as K (K-major)
-      const uint64_t v_desc = sdesc_sw128(ring_s, BN * 128, 1024);    // slot 0 read as V (MN-major)
+      // slot 0 read as V: MN-major (16-bit), or K-major V^T (e4m3)
+      const uint64_t v_desc = E8 ? sdesc_sw128(ring_s, 16, 1024) : sdesc_sw128(ring_s, BN * 128, 1024);
       uint32_t gL = 0, q_uses = 0;
       uint32_t pv_cnt[NQ], o_uses[NQ];
 #pragma unroll
@@ -357,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
           if (FA_ACTIVE(t, 0)) {
-            issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
+            issue_s<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS, E8>(tbase + C::s_col(t), q_desc, k_desc, t,
                                                                    gL % C::STAGES);
             umma_commit(&s_full[t]);
           }
@@ -386,8 +413,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
                 break;
               }
               tc_fence_after();
-              issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 16>(tbase + Cfg<D>::o_col(t),
-                                                                 tbase + Cfg<D>::s_col(t), v_desc,
+              issue_pv<D, BN, C::KV_BYTES, kIdO, E8>(tbase + C::o_col(t), tbase + C::s_col(t), v_desc,
                                                                  Lv % C::STAGES, !first);
               umma_commit(&o_full[t]);
               ++pv_cnt[t];
@@ -401,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
                 tc_fence_after();
                 k_ready = true;
               }
-              issue_s_tile<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS>(tbase + Cfg<D>::s_col(t), q_desc, k_desc, t,
+              issue_s<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS, E8>(tbase + C::s_col(t), q_desc, k_desc, t,
                                                                      Lk % C::STAGES);
               umma_commit(&s_full[t]);
             }
@@ -431,8 +457,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
     const int wq = warp & 3;
     const int r = 32 * wq + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
-    const uint32_t tS = tbase + lane_off + Cfg<D>::s_col(t);
-    const uint32_t tO = tbase + lane_off + Cfg<D>::o_col(t);
+    const uint32_t tS = tbase + lane_off + C::s_col(t);
+    const uint32_t tO = tbase + lane_off + C::o_col(t);
     const float sl2 = p.scale_log2;
     const bool split_mode = p.num_splits > 1;
     uint32_t gblk = 0;  // key blocks this tile has processed, over all items
@@ -441,6 +467,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       const int item = item_of(j);
       if (item >= total_items) break;
       int row0, n_top, it0, it_end, skv, off, left_off;
+      float sl2q = sl2;        // e4m3: the tile's Q scale folded into the score scale
+      const float* kd = nullptr;  // e4m3: the K scales of this head's key blocks
       {
         const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
         if (VARLEN && !w.valid) {
@@ -449,6 +477,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         }
         row0 = (w.m_cta * NQ + t) * BM;
         if (row0 >= w.sq) continue;  // no row of this tile in the sequence
+        if constexpr (E8) {  // (the tile exists: its scale index is below n_mtiles)
+          sl2q = sl2 * p.q_descale[(static_cast<int64_t>(w.bi) * p.hq + w.h) * p.n_mtiles + w.m_cta * NQ + t];
+          kd = p.k_descale + (static_cast<int64_t>(w.bi) * p.hkv + w.kvh) * p.n_kblocks;
+        }
         n_top = w.n_hi_max - 1;
         // (selects, not a runtime index: the arrays stay in registers)
         it0 = w.n_hi_max - (t == 0 ? w.n_hi[0] : w.n_hi[NQ - 1]);
@@ -467,6 +499,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
       int k = 0;
       for (int it = it0; it < it_end; ++it, ++gblk, ++k) {
         const int n = n_top - it;
+        // score scale of this block (the K scale load overlaps the wait for S)
+        float sl2b = sl2q;
+        if constexpr (E8) sl2b = sl2q * kd[n];
         if (!warp_wait(&s_full[t], gblk & 1, p.status, kSiteSFull)) {
           ok = false;
           break;
@@ -511,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         // The reference max moves only when the block max exceeds it by more than
         // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
         // unchanged); probabilities stay below 2^kRescaleLog2.
-        const float bm2 = bmax * sl2;
+        const float bm2 = bmax * sl2b;
         const bool grow = bm2 > m_run + kRescaleLog2;
         const float m_new = grow ? bm2 : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -538,11 +573,32 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         // P = 2^(s * scale * log2 e - m), written over the first half of the S
         // columns as packed 16-bit pairs; the MMA warp is signalled once per block
         // (a second, earlier signal for half of P measured slower).
-        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 sl2v = make_float2(sl2b, sl2b);
         const float2 negm = make_float2(-m_use, -m_use);
         float2 sum2[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
+        if constexpr (E8) {
+          // e4m3 P, four per column (P <= 2^kRescaleLog2 = 256 < 448, the largest e4m3)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[BN / 8];
+#pragma unroll
+            for (int c = 0; c < BN / 2; c += 4) {
+              const int cc = half * (BN / 2) + c;
+              const float2 x0 = __ffma2_rn(make_float2(s[cc], s[cc + 1]), sl2v, negm);
+              const float2 x1 = __ffma2_rn(make_float2(s[cc + 2], s[cc + 3]), sl2v, negm);
+              const float2 e0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+              const float2 e1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+              sum2[(c >> 2) & 3] = __fadd2_rn(sum2[(c >> 2) & 3], __fadd2_rn(e0, e1));
+              pk[c >> 2] = pack4_e4m3(e0.x, e0.y, e1.x, e1.y);
+            }
+            tmem_st16(tS + half * (BN / 8), pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_full[t]);
+        } else {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[BN / 4];
@@ -562,6 +618,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
             tc_fence_before();
             mbar_arrive(&p_full[t]);
           }
+        }
         }
         const float2 s01 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
         l_run = alpha * l_run + (s01.x + s01.y);
@@ -600,7 +657,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1) fa_prefill_kernel(const __
         break;
       }
       tc_fence_after();
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      // (e4m3: the V scale of the head applies to the whole accumulator)
+      const float vscale = E8 ? p.v_descale[static_cast<int64_t>(w.bi) * p.hkv + w.kvh] : 1.f;
+      const float inv_l = l_run > 0.f ? vscale / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
       // O leaves TMEM 32 columns at a time (the loads are warp-collective: every
       // lane executes them; only the global stores depend on the row existing)
@@ -689,6 +748,22 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+bool prefill_e4m3_supported(int d) { return d == 128; }
+
+cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stream) {
+  if (d != 128 || p.cu_q != nullptr || p.num_splits != 1) return cudaErrorInvalidValue;
+  using C = Cfg<128, true>;
+  auto kern = fa_prefill_kernel<128, true, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x3fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long grid = items < p.max_ctas ? items : p.max_ctas;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
 
 int prefill_block_n(int d) { return d <= 128 ? 128 : 64; }
 int prefill_q_tiles(int d) { return d <= 128 ? 2 : 1; }

@@ -94,4 +94,36 @@ __device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, 
   }
 }
 
+
+// 8-bit forms: S = Q K^T with e4m3 operands (D / 32 MMAs of K = 32, same 128-byte
+// swizzled K-major layout: a 128-byte row holds 128 elements) ...
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID>
+__device__ __forceinline__ void issue_s_tile_e4m3(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int q_slot,
+                                                  int slot) {
+  uint64_t qd = q_desc + static_cast<uint32_t>((q_slot * Q_BYTES) >> 4);
+  uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  asm volatile("" : "+l"(qd), "+l"(kd));
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) {
+    const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
+    const uint32_t offb = static_cast<uint32_t>(((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4);
+    umma_ss_f8(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
+  }
+}
+
+// ... and O (+)= P V with P e4m3 in TMEM (four per column, K = 32 per MMA = 8
+// columns) and V stored transposed ([d rows][keys], K-major, one 128-byte chunk of
+// BN = 128 keys per row).
+template <int D, int BN, int KV_BYTES, uint32_t ID>
+__device__ __forceinline__ void issue_pv_tile_e4m3(uint32_t o_tmem, uint32_t p_tmem, uint64_t vt_desc, int slot,
+                                                   bool acc) {
+  uint64_t vd = vt_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
+  asm volatile("" : "+l"(vd));
+#pragma unroll
+  for (int k = 0; k < BN / 32; ++k) {
+    const uint32_t off = static_cast<uint32_t>(((k >> 2) * (D * 128) + (k & 3) * 32) >> 4);
+    umma_ts_f8(o_tmem, p_tmem + k * 8, vd + off, ID, (acc || k > 0) ? 1u : 0u);
+  }
+}
+
 }  // namespace fa
