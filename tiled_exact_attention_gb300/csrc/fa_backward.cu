@@ -48,9 +48,12 @@ struct BwdCfg {
   static constexpr int BN = 128;             // keys per block
   static constexpr int DC = D / 64;          // 64-column chunks (128-byte rows)
   static constexpr int TILE_BYTES = 128 * D * 2;
-  static constexpr int THREADS = 256;        // 4 elementwise warps + producer + MMA + 2 idle
-  static constexpr int PRODUCER_WARP = 4;
-  static constexpr int MMA_WARP = 5;
+  // two elementwise warpgroups (each takes half of the columns of every block:
+  // nothing in the backward elementwise pass reduces along a row) + producer + MMA + 2 idle
+  static constexpr int THREADS = 384;
+  static constexpr int EW_THREADS = 256;
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
   static constexpr int TMEM_COLS = 512;
   // dQ kernel: Q and dO tiles, then a ring of K / V blocks
   static constexpr int DQ_STAGES = 4;
@@ -128,12 +131,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__
   }
 }
 
-// Store one row of D fp32 values (scaled by `mul`) from TMEM columns [col, col + D)
-// of this thread's lane to global memory as 16-bit values (when `valid`).
-template <int D, bool BF16>
+// Store NC fp32 values (scaled by `mul`) from TMEM columns [tcol, tcol + NC) of
+// this thread's lane to global memory as 16-bit values (when `valid`).
+template <int NC, bool BF16>
 __device__ __forceinline__ void store_acc_row(uint32_t tcol, float mul, uint16_t* dst, bool valid) {
 #pragma unroll
-  for (int c = 0; c < D; c += 32) {
+  for (int c = 0; c < NC; c += 32) {
     uint32_t v[32];
     tmem_load_row<32>(tcol + c, v);
     uint32_t pk[16];
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(ds_full, BM);
+    mbar_init(ds_full, C::EW_THREADS);
     mbar_init(dq_done, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -258,20 +261,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
         umma_commit(&kv_empty[Lv % ST]);
         if (!mbar_wait(ds_full, it & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
-        // dQ += dS K: dS from TMEM (over the S columns), K read MN-major
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, BN / 16>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc,
+        // dQ += dS K: dS from TMEM (keys 0..63 packed at S columns 0..31, keys 64..127
+        // at 64..95: each warpgroup packs into the columns it has read), K MN-major
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, BN / 32>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc,
                                                               Lk % ST, it > 0);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, BN / 32, BN / 16>(tbase + C::ACC_COL, tbase + C::S_COL + 32,
+                                                                    kmn_desc, Lk % ST, true);
         umma_commit(&kv_empty[Lk % ST]);
       }
       umma_commit(dq_done);
       mbar_wait(dq_done, 0, p.status, kSiteBwdDrain, true);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ---------------- elementwise: one query row per thread ----------------
-    const int r = 32 * warp + lane;
+  } else if (warp < 8) {
+    // ---------------- elementwise: one query row per thread, half of the keys per warpgroup ----------------
+    const int eg = warp >> 2;  // keys [64 eg, 64 eg + 64) of every block
+    const int r = 32 * (warp & 3) + lane;
     const int row = row0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tbase + lane_off + C::S_COL;
     const uint32_t tP = tbase + lane_off + C::DP_COL;
     const int64_t prow = (static_cast<int64_t>(bi) * p.hq + h) * p.sq_pad + row;  // row < sq_pad
@@ -291,7 +298,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       tc_fence_after();
       const int lim = lim_row - n * BN, lo = lo_row - n * BN;
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int cc = 0; cc < BN / 2; cc += 32) {
+        const int c0 = eg * (BN / 2) + cc;
         uint32_t sv[32], pv[32];
         tmem_load_row<32>(tS + c0, sv);
         tmem_load_row<32>(tP + c0, pv);
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
           }
           pk[i / 2] = pack2<BF16>(ds[0], ds[1]);
         }
-        tmem_st16(tS + c0 / 2, pk);
+        tmem_st16(tS + eg * (BN / 2) + cc / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -316,13 +324,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
     }
     uint16_t* dst = static_cast<uint16_t*>(p.dq) + bi * p.dq_st[0] + static_cast<int64_t>(row) * p.dq_st[1] +
                     h * p.dq_st[2];
+    // each warpgroup writes half of the row's d columns
     if (ok && N > 0 && warp_wait(dq_done, 0, p.status, kSiteBwdDone)) {
       tc_fence_after();
-      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL, p.scale, dst, row < p.sq);
+      store_acc_row<D / 2, BF16>(tbase + lane_off + C::ACC_COL + eg * (D / 2), p.scale, dst + eg * (D / 2),
+                                 row < p.sq);
     } else if (ok && N == 0 && row < p.sq) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      uint4* d4 = reinterpret_cast<uint4*>(dst + eg * (D / 2));
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < D / 16; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, BM);
+    mbar_init(p_full, C::EW_THREADS);
     mbar_init(mma_done, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&qd_full[s], 1);
@@ -446,21 +456,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
         if (!mbar_wait(p_full, ti & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
         // dV += P^T dO, dK += dS^T Q (P^T, dS^T from TMEM; dO, Q read MN-major)
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 16>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0,
+        // (query rows 0..63 packed at columns 0..31 of each region, rows 64..127 at 64..95)
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 32>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0,
                                                               ti > 0);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 16>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, BM / 32, BM / 16>(tbase + C::ACC_COL, tbase + C::S_COL + 32,
+                                                                    domn_desc, 0, true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 32>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
                                                               ti > 0);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, BM / 32, BM / 16>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 32,
+                                                                    qmn_desc, 0, true);
         umma_commit(&qd_empty[s]);
       }
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, p.status, kSiteBwdDrain, true);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ---------------- elementwise: one key per thread, query rows along the columns ----------------
-    const int r = 32 * warp + lane;
+    const int eg = warp >> 2;  // query rows [64 eg, 64 eg + 64) of every tile (the columns)
+    const int r = 32 * (warp & 3) + lane;
     const int j = j0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tbase + lane_off + C::S_COL;
     const uint32_t tP = tbase + lane_off + C::DP_COL;
     const float sl2 = p.scale_log2;
@@ -484,7 +500,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       if (p.causal) cmin = max(cmin, j - p.off - i0);        // j <= i + off
       if (p.local) cmax = min(cmax, j - p.left_off - i0);    // j >= i + left_off
 #pragma unroll
-      for (int c0 = 0; c0 < BM; c0 += 32) {
+      for (int cc = 0; cc < BM / 2; cc += 32) {
+        const int c0 = eg * (BM / 2) + cc;
         uint32_t sv[32], pv[32];
         tmem_load_row<32>(tS + c0, sv);
         tmem_load_row<32>(tP + c0, pv);
@@ -502,8 +519,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
           pp[i / 2] = pack2<BF16>(pr[0], pr[1]);
           pd[i / 2] = pack2<BF16>(ds[0], ds[1]);
         }
-        tmem_st16(tS + c0 / 2, pp);
-        tmem_st16(tP + c0 / 2, pd);
+        tmem_st16(tS + eg * (BM / 2) + cc / 2, pp);
+        tmem_st16(tP + eg * (BM / 2) + cc / 2, pd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -516,14 +533,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
                     kvh * p.dk_st[2];
     if (ok && T > 0 && warp_wait(mma_done, 0, p.status, kSiteBwdDone)) {
       tc_fence_after();
-      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL, 1.f, dvr, valid);
-      store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL + D, p.scale, dkr, valid);
+      // the first warpgroup writes dV, the second dK
+      if (eg == 0)
+        store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL, 1.f, dvr, valid);
+      else
+        store_acc_row<D, BF16>(tbase + lane_off + C::ACC_COL + D, p.scale, dkr, valid);
     } else if (ok && T == 0 && valid) {
       // no query row sees these keys: zero gradients
-      uint4* a = reinterpret_cast<uint4*>(dvr);
-      uint4* b = reinterpret_cast<uint4*>(dkr);
+      uint4* z = reinterpret_cast<uint4*>(eg == 0 ? dvr : dkr);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) a[c] = b[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < D / 8; ++c) z[c] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
