@@ -61,14 +61,14 @@ struct BwdCfg {
   static constexpr int DQ_BAR_OFF = DQ_RING_OFF + DQ_STAGES * TILE_BYTES;
   // (at least 117 KiB, so that one CTA, which holds all 512 TMEM columns, runs per SM)
   static constexpr int MIN_SMEM = 117 * 1024;
-  static constexpr int DQ_SMEM_RAW = DQ_BAR_OFF + 8 * (1 + 2 * DQ_STAGES + 3) + 16 + 1024;
+  static constexpr int DQ_SMEM_RAW = DQ_BAR_OFF + 8 * (1 + 2 * DQ_STAGES + 4) + 16 + 1024;
   static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
   // dK / dV kernel: K and V tiles, then stages of (Q tile, dO tile, L and D of their rows)
   static constexpr int KV_STAGES = 2;
   static constexpr int QD_STAGE_BYTES = 2 * TILE_BYTES + 1024;  // + 128 floats of L, 128 of D
   static constexpr int QD_OFF = 2 * TILE_BYTES;
   static constexpr int KV_BAR_OFF = QD_OFF + KV_STAGES * QD_STAGE_BYTES;
-  static constexpr int KV_SMEM_RAW = KV_BAR_OFF + 8 * (1 + 2 * KV_STAGES + 3) + 16 + 1024;
+  static constexpr int KV_SMEM_RAW = KV_BAR_OFF + 8 * (1 + 2 * KV_STAGES + 4) + 16 + 1024;
   static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
   static_assert(DQ_SMEM <= 227 * 1024 && KV_SMEM <= 227 * 1024, "shared memory budget");
   static_assert(QD_STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + ST;
   uint64_t* s_full = kv_empty + ST;   // S and dP of a block are in TMEM
-  uint64_t* ds_full = s_full + 1;     // dS of a block is in TMEM (count 128)
-  uint64_t* dq_done = ds_full + 1;    // every dQ MMA has completed
+  uint64_t* ds_half = s_full + 1;     // dS of the first / second half of a block's keys is in TMEM
+  uint64_t* dq_done = ds_half + 2;    // every dQ MMA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(ds_full, C::EW_THREADS);
+    mbar_init(&ds_half[0], C::EW_THREADS);
+    mbar_init(&ds_half[1], C::EW_THREADS);
     mbar_init(dq_done, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -259,14 +260,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
                                                                     Lv % ST);
         umma_commit(s_full);
         umma_commit(&kv_empty[Lv % ST]);
-        if (!mbar_wait(ds_full, it & 1, p.status, kSiteBwdDsFull)) break;
+        // dQ += dS K, half a block of keys at a time (the products of the first half run
+        // while the second half is formed): dS of keys [32 c, 32 c + 32) is packed at S
+        // columns [32 c, 32 c + 16), the first columns of the chunk its warp has read;
+        // K is read MN-major
+        if (!mbar_wait(&ds_half[0], it & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
-        // dQ += dS K: dS from TMEM (keys 0..63 packed at S columns 0..31, keys 64..127
-        // at 64..95: each warpgroup packs into the columns it has read), K MN-major
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, BN / 32>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc,
-                                                              Lk % ST, it > 0);
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, BN / 32, BN / 16>(tbase + C::ACC_COL, tbase + C::S_COL + 32,
-                                                                    kmn_desc, Lk % ST, true);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, 2>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc, Lk % ST,
+                                                        it > 0);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 2, 4>(tbase + C::ACC_COL, tbase + C::S_COL + 16, kmn_desc,
+                                                        Lk % ST, true);
+        if (!mbar_wait(&ds_half[1], it & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 4, 6>(tbase + C::ACC_COL, tbase + C::S_COL + 32, kmn_desc,
+                                                        Lk % ST, true);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 6, 8>(tbase + C::ACC_COL, tbase + C::S_COL + 48, kmn_desc,
+                                                        Lk % ST, true);
         umma_commit(&kv_empty[Lk % ST]);
       }
       umma_commit(dq_done);
@@ -297,9 +306,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       }
       tc_fence_after();
       const int lim = lim_row - n * BN, lo = lo_row - n * BN;
+      // chunk of 32 keys: warpgroup eg takes chunk eg of each half; the half is
+      // signalled once both warpgroups have packed their chunk
 #pragma unroll
-      for (int cc = 0; cc < BN / 2; cc += 32) {
-        const int c0 = eg * (BN / 2) + cc;
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = hf * (BN / 2) + eg * 32;
         uint32_t sv[32], pv[32];
         tmem_load_row<32>(tS + c0, sv);
         tmem_load_row<32>(tP + c0, pv);
@@ -316,11 +327,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
           }
           pk[i / 2] = pack2<BF16>(ds[0], ds[1]);
         }
-        tmem_st16(tS + eg * (BN / 2) + cc / 2, pk);
+        tmem_st16(tS + c0, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_half[hf]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ds_full);
     }
     uint16_t* dst = static_cast<uint16_t*>(p.dq) + bi * p.dq_st[0] + static_cast<int64_t>(row) * p.dq_st[1] +
                     h * p.dq_st[2];
@@ -368,8 +379,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   uint64_t* qd_full = kv_full + 1;   // per stage: Q, dO, L2, D of a query tile landed
   uint64_t* qd_empty = qd_full + ST;
   uint64_t* s_full = qd_empty + ST;  // S^T and dP^T in TMEM
-  uint64_t* p_full = s_full + 1;     // P^T and dS^T in TMEM (count 128)
-  uint64_t* mma_done = p_full + 1;
+  uint64_t* p_half = s_full + 1;     // P^T and dS^T of the first / second half of a tile's rows in TMEM
+  uint64_t* mma_done = p_half + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   auto stage_ptr = [&](int s) { return smem + C::QD_OFF + s * C::QD_STAGE_BYTES; };
 
@@ -386,7 +397,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_full, C::EW_THREADS);
+    mbar_init(&p_half[0], C::EW_THREADS);
+    mbar_init(&p_half[1], C::EW_THREADS);
     mbar_init(mma_done, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&qd_full[s], 1);
@@ -453,18 +465,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
         issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, k_desc, qk_desc, 0, 0);
         issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, v_desc, dok_desc, 0, 0);
         umma_commit(s_full);
-        if (!mbar_wait(p_full, ti & 1, p.status, kSiteBwdDsFull)) break;
+        // dV += P^T dO, dK += dS^T Q, half a tile of query rows at a time (the products
+        // of the first half run while the second half is formed); P^T / dS^T of rows
+        // [32 c, 32 c + 32) are packed at columns [32 c, 32 c + 16) of their region;
+        // dO and Q are read MN-major
+        if (!mbar_wait(&p_half[0], ti & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q (P^T, dS^T from TMEM; dO, Q read MN-major)
-        // (query rows 0..63 packed at columns 0..31 of each region, rows 64..127 at 64..95)
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 32>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0,
-                                                              ti > 0);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, BM / 32, BM / 16>(tbase + C::ACC_COL, tbase + C::S_COL + 32,
-                                                                    domn_desc, 0, true);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, BM / 32>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
-                                                              ti > 0);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, BM / 32, BM / 16>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 32,
-                                                                    qmn_desc, 0, true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, 2>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0, ti > 0);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 2, 4>(tbase + C::ACC_COL, tbase + C::S_COL + 16, domn_desc, 0,
+                                                        true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, 2>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
+                                                        ti > 0);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 2, 4>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 16, qmn_desc, 0,
+                                                        true);
+        if (!mbar_wait(&p_half[1], ti & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 4, 6>(tbase + C::ACC_COL, tbase + C::S_COL + 32, domn_desc, 0,
+                                                        true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 6, 8>(tbase + C::ACC_COL, tbase + C::S_COL + 48, domn_desc, 0,
+                                                        true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 4, 6>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 32, qmn_desc, 0,
+                                                        true);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 6, 8>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 48, qmn_desc, 0,
+                                                        true);
         umma_commit(&qd_empty[s]);
       }
       umma_commit(mma_done);
@@ -500,8 +523,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       if (p.causal) cmin = max(cmin, j - p.off - i0);        // j <= i + off
       if (p.local) cmax = min(cmax, j - p.left_off - i0);    // j >= i + left_off
 #pragma unroll
-      for (int cc = 0; cc < BM / 2; cc += 32) {
-        const int c0 = eg * (BM / 2) + cc;
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = hf * (BM / 2) + eg * 32;  // warpgroup eg takes chunk eg of each half
         uint32_t sv[32], pv[32];
         tmem_load_row<32>(tS + c0, sv);
         tmem_load_row<32>(tP + c0, pv);
@@ -519,12 +542,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
           pp[i / 2] = pack2<BF16>(pr[0], pr[1]);
           pd[i / 2] = pack2<BF16>(ds[0], ds[1]);
         }
-        tmem_st16(tS + eg * (BM / 2) + cc / 2, pp);
-        tmem_st16(tP + eg * (BM / 2) + cc / 2, pd);
+        tmem_st16(tS + c0, pp);
+        tmem_st16(tP + c0, pd);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_half[hf]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
     }
     const bool valid = j < p.skv;
     uint16_t* dvr = static_cast<uint16_t*>(p.dv) + bi * p.dv_st[0] + static_cast<int64_t>(j) * p.dv_st[1] +
