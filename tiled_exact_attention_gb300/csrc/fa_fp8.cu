@@ -3,12 +3,15 @@
 // so that a few large values do not crush the precision of the whole block, and
 // the scales carried into the computation).
 //
-// Two kernels per tensor, both bound by HBM:
-//   * fa_amax_kernel: the largest |x| of each 128-row block of one (batch, head),
-//     or of the whole (batch, head); descale = amax / 448 (448 is the largest
-//     finite e4m3 value; an all-zero block gets descale 1);
-//   * fa_quant_kernel: code = round-to-nearest-even e4m3 of x * (1 / descale),
-//     saturating, written row-major or transposed ([d][rows], for V).
+// Per tensor, bound by HBM:
+//   * fa_amax_kernel (one CTA per 128-row block of one (batch, head)): the block's
+//     largest |x|, max-reduced into its scale slot (one slot per block, or one per
+//     (batch, head) shared by its blocks: an integer atomic max on the bits of a
+//     non-negative float orders like the float);
+//   * fa_quant_kernel: descale = amax / 448 (448 is the largest finite e4m3 value;
+//     an all-zero block gets 1), code = round-to-nearest-even e4m3 of
+//     x * (1 / descale), saturating, written row-major or transposed ([d][rows], for V);
+//   * fa_descale_kernel: the slots turn from amax into descale.
 // The products use IEEE round-to-nearest (division, reciprocal, multiplication
 // written with the _rn intrinsics), so a CPU check reproduces every code bit for bit.
 #include <cuda_bf16.h>
@@ -31,16 +34,21 @@ __device__ __forceinline__ float to_f32(uint16_t u) {
   }
 }
 
-// One CTA of 256 threads per scale: rows [r0, r1) of (batch, head), d columns.
+__device__ __forceinline__ float descale_of(float amax) { return amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f; }
+
+__device__ __forceinline__ int64_t scale_slot(const QuantParams& p, int bh, int blk) {
+  return p.per_head ? bh : static_cast<int64_t>(bh) * p.nblk + blk;
+}
+
+// One CTA of 256 threads per 128-row block of one (batch, head); the slots start at 0.
 template <bool BF16>
 __global__ void __launch_bounds__(256) fa_amax_kernel(const __grid_constant__ QuantParams p) {
   __shared__ float red[8];
-  const int nscale = p.per_head ? 1 : p.nblk;
-  const int blk = blockIdx.x % nscale;
-  const int bh = blockIdx.x / nscale;
+  const int blk = blockIdx.x % p.nblk;
+  const int bh = blockIdx.x / p.nblk;
   const int h = bh % p.h, bi = bh / p.h;
-  const int r0 = p.per_head ? 0 : blk * 128;
-  const int r1 = p.per_head ? p.s : min(p.s, r0 + 128);
+  const int r0 = blk * 128;
+  const int r1 = min(p.s, r0 + 128);
   const int vec = p.d / 8;  // 16-byte pieces per row
   float m = 0.f;
   for (int64_t i = threadIdx.x; i < static_cast<int64_t>(r1 - r0) * vec; i += 256) {
@@ -61,8 +69,14 @@ __global__ void __launch_bounds__(256) fa_amax_kernel(const __grid_constant__ Qu
   if (threadIdx.x == 0) {
     float a = red[0];
     for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-    p.descale[static_cast<int64_t>(bh) * nscale + blk] = a > 0.f ? __fdiv_rn(a, kE4m3Max) : 1.f;
+    atomicMax(reinterpret_cast<int*>(p.descale + scale_slot(p, bh, blk)), __float_as_int(a));
   }
+}
+
+// The slots hold amax; make them descales.
+__global__ void __launch_bounds__(256) fa_descale_kernel(float* slots, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n; i += static_cast<int64_t>(gridDim.x) * 256)
+    slots[i] = descale_of(slots[i]);
 }
 
 // One CTA of 256 threads per 128-row block of one (batch, head).
@@ -74,7 +88,7 @@ __global__ void __launch_bounds__(256) fa_quant_kernel(const __grid_constant__ Q
   const int h = bh % p.h, bi = bh / p.h;
   const int r0 = blk * 128;
   const int rows = min(128, p.s - r0);
-  const float ds = p.descale[p.per_head ? bh : static_cast<int64_t>(bh) * p.nblk + blk];
+  const float ds = descale_of(p.descale[scale_slot(p, bh, blk)]);  // (the slot holds amax until the end)
   const float inv = __frcp_rn(ds);
   const int vec = p.d / 8;
   for (int i = threadIdx.x; i < rows * vec; i += 256) {
@@ -120,18 +134,21 @@ __global__ void __launch_bounds__(256) fa_quant_kernel(const __grid_constant__ Q
 
 template <bool BF16>
 cudaError_t launch_quant_t(const QuantParams& p, cudaStream_t stream) {
-  const int64_t nscale = p.per_head ? 1 : p.nblk;
-  const int64_t g1 = static_cast<int64_t>(p.b) * p.h * nscale;
-  const int64_t g2 = static_cast<int64_t>(p.b) * p.h * p.nblk;
-  if (g1 <= 0 || g2 <= 0) return cudaSuccess;
-  if (g2 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fa_amax_kernel<BF16><<<static_cast<unsigned>(g1), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const int64_t nslots = static_cast<int64_t>(p.b) * p.h * (p.per_head ? 1 : p.nblk);
+  const int64_t g = static_cast<int64_t>(p.b) * p.h * p.nblk;
+  if (g <= 0) return cudaSuccess;
+  if (g > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaMemsetAsync(p.descale, 0, static_cast<size_t>(nslots) * sizeof(float), stream);
   if (e != cudaSuccess) return e;
+  fa_amax_kernel<BF16><<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.transpose)
-    fa_quant_kernel<BF16, true><<<static_cast<unsigned>(g2), 256, 0, stream>>>(p);
+    fa_quant_kernel<BF16, true><<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
   else
-    fa_quant_kernel<BF16, false><<<static_cast<unsigned>(g2), 256, 0, stream>>>(p);
+    fa_quant_kernel<BF16, false><<<static_cast<unsigned>(g), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t g3 = (nslots + 255) / 256;
+  fa_descale_kernel<<<static_cast<unsigned>(g3 < 1024 ? g3 : 1024), 256, 0, stream>>>(p.descale, nslots);
   return cudaGetLastError();
 }
 
