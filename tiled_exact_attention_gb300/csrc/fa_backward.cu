@@ -79,54 +79,78 @@ struct BwdCfg {
 
 // ------------------------------------------------------------------ preprocess
 
-// One warp per (batch, head, padded row): D = sum_t dO_t O_t in fp32 from the
-// stored (rounded) O, and L2 = LSE * log2(e); padding rows and rows that see no
-// key get L2 = +inf, so that every probability recovered from it is 0.
+// D = sum_t dO_t O_t in fp32 from the stored (rounded) O, and L2 = LSE * log2(e),
+// per (batch, head, padded row); padding rows and rows that see no key get
+// L2 = +inf, so that every probability recovered from it is 0.  D / 8 lanes per
+// row with 16-byte loads, several rows per warp in flight (the pass is bound by
+// HBM, not by its arithmetic).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
-  constexpr int EPL = D / 32;  // elements per lane
+  constexpr int LPR = D / 8;        // lanes per row
+  constexpr int RPW = 32 / LPR;     // rows per warp per step
+  constexpr int UNROLL = 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR, li = lane % LPR;
   const int64_t nrows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp; row < nrows;
-       row += static_cast<int64_t>(gridDim.x) * 8) {
-    const int i = static_cast<int>(row % p.sq_pad);
-    const int64_t bh = row / p.sq_pad;
-    const int h = static_cast<int>(bh % p.hq), bi = static_cast<int>(bh / p.hq);
-    float dsum = 0.f, l2 = INFINITY;
-    if (i < p.sq) {
-      const uint16_t* orow = static_cast<const uint16_t*>(p.o) + bi * p.o_st[0] + static_cast<int64_t>(i) * p.o_st[1] +
-                             h * p.o_st[2] + lane * EPL;
-      const uint16_t* drow = static_cast<const uint16_t*>(p.dout) + bi * p.do_st[0] +
-                             static_cast<int64_t>(i) * p.do_st[1] + h * p.do_st[2] + lane * EPL;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * 8 * RPW * UNROLL;
+  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * RPW * UNROLL; base < nrows; base += step) {
+    float dsum[UNROLL], l2[UNROLL];
+    uint4 ou[UNROLL], du[UNROLL];
+    int64_t rowid[UNROLL];
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const uint32_t ou = *reinterpret_cast<const uint32_t*>(orow + e);
-        const uint32_t du = *reinterpret_cast<const uint32_t*>(drow + e);
+    for (int u = 0; u < UNROLL; ++u) {
+      const int64_t row = base + u * RPW + sub;
+      rowid[u] = row;
+      ou[u] = du[u] = make_uint4(0u, 0u, 0u, 0u);
+      l2[u] = INFINITY;
+      if (row < nrows) {
+        const int i = static_cast<int>(row % p.sq_pad);
+        const int64_t bh = row / p.sq_pad;
+        const int h = static_cast<int>(bh % p.hq), bi = static_cast<int>(bh / p.hq);
+        if (i < p.sq) {
+          ou[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + bi * p.o_st[0] +
+                                                  static_cast<int64_t>(i) * p.o_st[1] + h * p.o_st[2] + li * 8);
+          du[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + bi * p.do_st[0] +
+                                                  static_cast<int64_t>(i) * p.do_st[1] + h * p.do_st[2] + li * 8);
+          const float lse = p.lse[bh * p.sq + i];
+          l2[u] = lse > -INFINITY ? lse * kLog2e : INFINITY;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const uint32_t ow[4] = {ou[u].x, ou[u].y, ou[u].z, ou[u].w};
+      const uint32_t dw[4] = {du[u].x, du[u].y, du[u].z, du[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         float o0, o1, d0, d1;
         if constexpr (BF16) {
-          o0 = __uint_as_float(ou << 16);
-          o1 = __uint_as_float(ou & 0xffff0000u);
-          d0 = __uint_as_float(du << 16);
-          d1 = __uint_as_float(du & 0xffff0000u);
+          o0 = __uint_as_float(ow[e] << 16);
+          o1 = __uint_as_float(ow[e] & 0xffff0000u);
+          d0 = __uint_as_float(dw[e] << 16);
+          d1 = __uint_as_float(dw[e] & 0xffff0000u);
         } else {
-          const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ou));
-          const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&du));
+          const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[e]));
+          const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&dw[e]));
           o0 = of.x;
           o1 = of.y;
           d0 = df.x;
           d1 = df.y;
         }
-        dsum = fmaf(o0, d0, dsum);
-        dsum = fmaf(o1, d1, dsum);
+        acc = fmaf(o0, d0, acc);
+        acc = fmaf(o1, d1, acc);
       }
 #pragma unroll
-      for (int x = 16; x > 0; x >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, x);
-      const float lse = p.lse[(static_cast<int64_t>(bi) * p.hq + h) * p.sq + i];
-      l2 = lse > -INFINITY ? lse * kLog2e : INFINITY;
+      for (int x = LPR / 2; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+      dsum[u] = acc;
     }
-    if (lane == 0) {
-      p.dpre[row] = dsum;
-      p.l2pre[row] = l2;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      if (li == 0 && rowid[u] < nrows) {
+        p.dpre[rowid[u]] = dsum[u];
+        p.l2pre[rowid[u]] = l2[u];
+      }
     }
   }
 }
@@ -582,7 +606,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   {
     const int64_t rows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
-    const int64_t blocks = (rows + 7) / 8;
+    const int64_t blocks = (rows + 8 * 2 * (256 / D) - 1) / (8 * 2 * (256 / D));  // rows per CTA step
     const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
     if (grid > 0) fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
