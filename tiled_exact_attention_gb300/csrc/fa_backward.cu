@@ -54,6 +54,11 @@ struct BwdCfg {
   static constexpr int EW_THREADS = 256;
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
+  // register split: launched at 168 per thread (384 threads); the control warpgroup
+  // drops to 72 and the elementwise warpgroups rise to 208: 256 * 208 + 128 * 72 <= 384 * 168
+  static constexpr int REG_EW = 208;
+  static constexpr int REG_CONTROL = 72;
+  static_assert(EW_THREADS * REG_EW + 128 * REG_CONTROL <= THREADS * 168, "register split");
   static constexpr int TMEM_COLS = 512;
   // dQ kernel: Q and dO tiles, then a ring of K / V blocks
   static constexpr int DQ_STAGES = 4;
@@ -236,6 +241,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= 8) {
+    // control warpgroup (producer, MMA issuer, two idle warps): registers move to the elementwise warps
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_CONTROL));
   if (warp == C::PRODUCER_WARP) {
     if (lane == 0 && N > 0) {
       mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
@@ -306,7 +314,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       mbar_wait(dq_done, 0, p.status, kSiteBwdDrain, true);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_EW));
     // ---------------- elementwise: one query row per thread, half of the keys per warpgroup ----------------
     const int eg = warp >> 2;  // keys [64 eg, 64 eg + 64) of every block
     const int r = 32 * (warp & 3) + lane;
@@ -332,12 +342,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       const int lim = lim_row - n * BN, lo = lo_row - n * BN;
       // chunk of 32 keys: warpgroup eg takes chunk eg of each half; the half is
       // signalled once both warpgroups have packed their chunk
+      // both chunks of this warpgroup loaded at once (the second load's latency hides
+      // behind the first chunk's arithmetic)
+      uint32_t sv2[2][32], pv2[2][32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tmem_ld32_issue(tS + hf * (BN / 2) + eg * 32, sv2[hf]);
+        tmem_ld32_issue(tP + hf * (BN / 2) + eg * 32, pv2[hf]);
+      }
+      tmem_ld_wait();
+      reg_fence<32>(sv2[0]);
+      reg_fence<32>(sv2[1]);
+      reg_fence<32>(pv2[0]);
+      reg_fence<32>(pv2[1]);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = hf * (BN / 2) + eg * 32;
-        uint32_t sv[32], pv[32];
-        tmem_load_row<32>(tS + c0, sv);
-        tmem_load_row<32>(tP + c0, pv);
+        const uint32_t* sv = sv2[hf];
+        const uint32_t* pv = pv2[hf];
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -439,6 +461,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp >= 8) {
+    // control warpgroup (producer, MMA issuer, two idle warps): registers move to the elementwise warps
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_CONTROL));
   if (warp == C::PRODUCER_WARP) {
     if (lane == 0 && T > 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
@@ -518,7 +543,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       mbar_wait(mma_done, 0, p.status, kSiteBwdDrain, true);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_EW));
     // ---------------- elementwise: one key per thread, query rows along the columns ----------------
     const int eg = warp >> 2;  // query rows [64 eg, 64 eg + 64) of every tile (the columns)
     const int r = 32 * (warp & 3) + lane;
@@ -546,25 +573,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       if (j >= p.skv) cmin = BM;  // a key past the end: nothing
       if (p.causal) cmin = max(cmin, j - p.off - i0);        // j <= i + off
       if (p.local) cmax = min(cmax, j - p.left_off - i0);    // j >= i + left_off
+      // both chunks of this warpgroup (one per half) are loaded at once, so the
+      // second load's latency hides behind the first chunk's arithmetic
+      uint32_t sv[2][32], pv[2][32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tmem_ld32_issue(tS + hf * (BM / 2) + eg * 32, sv[hf]);
+        tmem_ld32_issue(tP + hf * (BM / 2) + eg * 32, pv[hf]);
+      }
+      tmem_ld_wait();
+      reg_fence<32>(sv[0]);
+      reg_fence<32>(sv[1]);
+      reg_fence<32>(pv[0]);
+      reg_fence<32>(pv[1]);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = hf * (BM / 2) + eg * 32;  // warpgroup eg takes chunk eg of each half
-        uint32_t sv[32], pv[32];
-        tmem_load_row<32>(tS + c0, sv);
-        tmem_load_row<32>(tP + c0, pv);
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pr[2], ds[2];
+        for (int i = 0; i < 32; i += 4) {
+          // L2 and D of four query rows at once (the same address in every lane)
+          const float4 l4 = *reinterpret_cast<const float4*>(l2v + c0 + i);
+          const float4 d4 = *reinterpret_cast<const float4*>(dv + c0 + i);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], ds[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
+          for (int e = 0; e < 4; ++e) {
             const int c = c0 + i + e;
             const bool vis = c >= cmin && c <= cmax;
-            pr[e] = vis ? ex2_approx(__uint_as_float(sv[i + e]) * sl2 - l2v[c]) : 0.f;
-            ds[e] = pr[e] * (__uint_as_float(pv[i + e]) - dv[c]);
+            pr[e] = vis ? ex2_approx(__uint_as_float(sv[hf][i + e]) * sl2 - lv[e]) : 0.f;
+            ds[e] = pr[e] * (__uint_as_float(pv[hf][i + e]) - dvv[e]);
           }
           pp[i / 2] = pack2<BF16>(pr[0], pr[1]);
+          pp[i / 2 + 1] = pack2<BF16>(pr[2], pr[3]);
           pd[i / 2] = pack2<BF16>(ds[0], ds[1]);
+          pd[i / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
         }
         tmem_st16(tS + c0, pp);
         tmem_st16(tP + c0, pd);
