@@ -360,18 +360,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
         const int c0 = hf * (BN / 2) + eg * 32;
         const uint32_t* sv = sv2[hf];
         const uint32_t* pv = pv2[hf];
+        const bool edge = lim < c0 + 32 || lo > c0;
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = c0 + i + e;
-            const bool vis = c < lim && c >= lo;
-            const float pr = vis ? ex2_approx(__uint_as_float(sv[i + e]) * sl2 - l2) : 0.f;
-            ds[e] = pr * (__uint_as_float(pv[i + e]) - dd);
+          // pairs of keys in packed f32x2 math; the mask only where an edge cuts the chunk
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                                      make_float2(sl2, sl2), make_float2(-l2, -l2));
+          float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (edge) {
+            const int c = c0 + i;
+            if (c >= lim || c < lo) pr.x = 0.f;
+            if (c + 1 >= lim || c + 1 < lo) pr.y = 0.f;
           }
-          pk[i / 2] = pack2<BF16>(ds[0], ds[1]);
+          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
+                                                      make_float2(-dd, -dd)));
+          pk[i / 2] = pack2<BF16>(ds.x, ds.y);
         }
         tmem_st16(tS + c0, pk);
         tmem_st_wait();
@@ -591,23 +595,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
         const int c0 = hf * (BM / 2) + eg * 32;  // warpgroup eg takes chunk eg of each half
         uint32_t pp[16], pd[16];
 #pragma unroll
+        // the mask only where an edge cuts this chunk; pairs of columns in packed f32x2 math
+        const bool edge = cmin > c0 || cmax < c0 + 31;
+        const float2 sl2v = make_float2(sl2, sl2);
         for (int i = 0; i < 32; i += 4) {
           // L2 and D of four query rows at once (the same address in every lane)
           const float4 l4 = *reinterpret_cast<const float4*>(l2v + c0 + i);
           const float4 d4 = *reinterpret_cast<const float4*>(dv + c0 + i);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], ds[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c0 + i + e;
-            const bool vis = c >= cmin && c <= cmax;
-            pr[e] = vis ? ex2_approx(__uint_as_float(sv[hf][i + e]) * sl2 - lv[e]) : 0.f;
-            ds[e] = pr[e] * (__uint_as_float(pv[hf][i + e]) - dvv[e]);
+          for (int e = 0; e < 4; e += 2) {
+            const float2 nl = e == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
+            const float2 nd = e == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[hf][i + e]), __uint_as_float(sv[hf][i + e + 1])),
+                                        sl2v, nl);
+            float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (edge) {
+              const int c = c0 + i + e;
+              if (c < cmin || c > cmax) pr.x = 0.f;
+              if (c + 1 < cmin || c + 1 > cmax) pr.y = 0.f;
+            }
+            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(pv[hf][i + e]), __uint_as_float(pv[hf][i + e + 1])), nd);
+            const float2 ds = __fmul2_rn(pr, dpd);
+            pp[(i + e) / 2] = pack2<BF16>(pr.x, pr.y);
+            pd[(i + e) / 2] = pack2<BF16>(ds.x, ds.y);
           }
-          pp[i / 2] = pack2<BF16>(pr[0], pr[1]);
-          pp[i / 2 + 1] = pack2<BF16>(pr[2], pr[3]);
-          pd[i / 2] = pack2<BF16>(ds[0], ds[1]);
-          pd[i / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
         }
         tmem_st16(tS + c0, pp);
         tmem_st16(tP + c0, pd);
