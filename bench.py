@@ -2,7 +2,8 @@
 
 One step = one pass of the whole path over one batch of synthetic input:
   * causal prefill forward (fa_fwd) on B=4, Hq=Hkv=16, N=4096, d=128, bf16;
-  * split-KV decode (fa_fwd_splitkv: split kernel + LSE-weighted combine) on
+  * split-KV decode (fa_fwd_splitkv: one split kernel whose last CTA per head
+    group merges the splits' partials, LSE-weighted) on
     B=8, Hq=32, Hkv=8, KV length 32768, d=128, bf16, query position 32767.
 `value` is the prefill's forward TFLOP/s (4 * d * visible (query, key) pairs *
 b * hq per launch, over that launch's CUDA-event time); the decode's KV GB/s is
@@ -318,7 +319,7 @@ def run_ours(args):
                          "frac": round(dec_gbs / hbm, 4), "peak_source": peak_src,
                          "traffic": dec_traffic, "spec_peak": 8000.0,
                          "frac_of_spec": round(dec_gbs / 8000.0, 4),
-                         "note": "phase time = split kernel + combine kernel"},
+                         "note": "phase time = split kernel with the fused merge (+ a memset of its counters)"},
         },
         "decode_paged": dict(paged, roofline={"bound": "hbm", "achieved": paged["value"], "peak": hbm,
                                               "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
@@ -340,7 +341,7 @@ def run_ours(args):
         "e2e": {"value": round(job_throughput(flops, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step"},
-        "gpu_launches": K * 3,
+        "gpu_launches": K * 2,
         "wall_s_timed_region": round(wall, 3),
     }
     if not args.no_cpu_baseline:

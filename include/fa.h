@@ -125,8 +125,9 @@ int32_t fa_splitkv_default_splits(const fa_fwd_args* args);
 /*
  * Workspace bytes fa_fwd_splitkv needs for `num_splits` splits (0 = the
  * default count): fp32 partial outputs [num_splits, b, hq, sq, d] followed
- * (256-byte aligned) by fp32 partial LSEs [num_splits, b, hq, sq].
- * Returns 0 for invalid arguments.
+ * (256-byte aligned) by fp32 partial LSEs [num_splits, b, hq, sq] and
+ * (256-byte aligned) b * hq int32 merge counters, which the call zeroes itself
+ * on the stream before it uses them.  Returns 0 for invalid arguments.
  */
 size_t fa_splitkv_workspace_size(const fa_fwd_args* args, int32_t num_splits);
 
@@ -136,9 +137,11 @@ size_t fa_splitkv_workspace_size(const fa_fwd_args* args, int32_t num_splits);
  * compute_attn_1rowblock_splitkv): the key blocks are cut into num_splits
  * contiguous ranges of ceil(nblk / num_splits) blocks; split s writes its
  * normalised partial O_s and LSE_s into the workspace (0 and -inf for a split
- * with no visible key), then fa_splitkv_combine merges them into args->o and
- * args->lse.  For sq == 1 the query heads sharing a KV head are folded into
- * one CTA (section 7.4).  num_splits == 0 picks the count with the heuristic;
+ * with no visible key), then they are merged into args->o and args->lse as
+ * fa_splitkv_combine does: for sq > 1 by that kernel, for sq == 1 inside the
+ * split kernel (the last split of each head group to finish merges them; one
+ * launch plus a small memset of the counters).  For sq == 1 the query heads
+ * sharing a KV head are folded into one CTA (section 7.4).  num_splits == 0 picks the count with the heuristic;
  * the count used is written to *splits_used (may be NULL).  The workspace is a
  * caller-owned device buffer of at least fa_splitkv_workspace_size bytes,
  * 256-byte aligned.  Same result as fa_fwd up to rounding.
@@ -215,7 +218,8 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits
  * same split kernel and LSE-weighted combine as fa_fwd_splitkv, with the key
  * blocks of each sequence addressed through its block table or its prefix sum
  * and cut into num_splits ranges of that sequence's own length (0 = the
- * split-count heuristic, applied with max_seqlen_k).  The workspace is caller-owned device memory of at least
+ * split-count heuristic, applied with max_seqlen_k), merged inside the split
+ * kernel as for fa_fwd_splitkv with sq == 1.  The workspace is caller-owned device memory of at least
  * fa_kvcache_workspace_size bytes, 256-byte aligned.
  */
 fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,

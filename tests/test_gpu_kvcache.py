@@ -58,6 +58,11 @@ PAGED = [
     (2, 32, 8, 128, "bf16", 128, [2049, 6000], 1),
     (4, 4, 4, 64, "fp16", 128, [129, 64, 1000, 7], 0),
     (2, 8, 1, 256, "bf16", 64, [500, 1500], 2),
+    # pages smaller than the 128-key block, or not a multiple of it: a block is
+    # loaded as 64-row boxes from different pages
+    (2, 8, 2, 128, "bf16", 192, [1000, 385], 0),
+    (3, 4, 2, 64, "fp16", 64, [300, 129, 64], 2),
+    (2, 8, 2, 128, "bf16", 320, [641, 1279], 3),
 ]
 
 

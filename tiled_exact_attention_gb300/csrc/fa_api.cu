@@ -241,9 +241,13 @@ bool noalloc_scratch(void** out) {
   return true;
 }
 
+// Merge counters of the fused split-KV decode: one int per (batch, query-head
+// group), at most one per (batch, query head).
+size_t counters_bytes(int b, int hq) { return align256(static_cast<size_t>(b) * hq * sizeof(int)); }
+
 size_t workspace_bytes_for(const fa_fwd_args* a, int ns) {
   const size_t rows = static_cast<size_t>(ns) * a->b * a->hq * a->sq;
-  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
+  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float)) + counters_bytes(a->b, a->hq);
 }
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
@@ -268,7 +272,7 @@ fa_status validate_kvcache(const fa_kvcache_args* a) {
     return FA_ERR_INVALID_ARG;
   if (!strides_pos(a->q_strides, 2) || !strides_pos(a->o_strides, 2)) return FA_ERR_INVALID_ARG;
   if (a->page_size > 0) {
-    if (a->page_size % decode_block_n(a->d) != 0) return FA_ERR_UNSUPPORTED;
+    if (a->page_size % 64 != 0) return FA_ERR_UNSUPPORTED;
     if (a->block_table == nullptr || a->seqlens_k == nullptr || a->block_table_stride < 1) return FA_ERR_INVALID_ARG;
     if (!aligned(a->block_table, 4) || !aligned(a->seqlens_k, 4)) return FA_ERR_INVALID_ARG;
     if (!strides_ok(a->k_strides) || !strides_ok(a->v_strides)) return FA_ERR_INVALID_ARG;
@@ -514,7 +518,17 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     p.blocks_per_split = static_cast<int>(ceil_div64(span > 0 ? span : 1, ns));
     p.scale_log2 = scale_log2;
     p.status = di.status;
-    e = launch_decode(p, a->d, a->dtype, st);
+    p.box_rows = bn;
+    p.counters = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(lse_part) + align256(rows * sizeof(float)));
+    p.o = a->o;
+    p.o_stride_b = a->o_strides[0];
+    p.o_stride_h = a->o_strides[2];
+    p.lse = a->lse;
+    e = cudaMemsetAsync(p.counters, 0, counters_bytes(a->b, a->hq), st);
+    if (e == cudaSuccess) e = launch_decode(p, a->d, a->dtype, st);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (splits_used) *splits_used = ns;
+    return FA_OK;  // the decode kernel merges the splits itself
   } else {
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
@@ -581,7 +595,7 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
   if (!device_info(&di)) return FA_ERR_CUDA;
   const int ns = kvcache_splits(a, num_splits, di);
   const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
-  const size_t need = align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
+  const size_t need = align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float)) + counters_bytes(a->b, a->hq);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * a->d * sizeof(float)));
@@ -596,8 +610,10 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
                            a->v_strides[1], a->v_strides[2]};
   const int rows_dim = paged ? a->page_size : a->num_pages;
   const int outer_dim = paged ? a->num_pages : 1;
-  if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, rows_dim, outer_dim, k_st, a->d, bn, false) ||
-      !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, rows_dim, outer_dim, v_st, a->d, bn, false))
+  // a block of bn keys is loaded as boxes that never straddle a page
+  const int box_rows = (!paged || a->page_size % bn == 0) ? bn : 64;
+  if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, rows_dim, outer_dim, k_st, a->d, box_rows, false) ||
+      !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, rows_dim, outer_dim, v_st, a->d, box_rows, false))
     return FA_ERR_INVALID_ARG;
   p.q = a->q;
   p.q_stride_b = a->q_strides[0];
@@ -621,13 +637,19 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
   p.block_table = a->block_table;
   p.bt_stride = a->block_table_stride;
   p.page_size = a->page_size;
+  p.box_rows = box_rows;
   p.seqlens = a->seqlens_k;
   p.cu_seqlens = a->cu_seqlens_k;
+  p.counters = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(lse_part) + align256(rows * sizeof(float)));
+  p.o = a->o;
+  p.o_stride_b = a->o_strides[0];
+  p.o_stride_h = a->o_strides[1];
+  p.lse = a->lse;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(p.counters, 0, counters_bytes(a->b, a->hq), st) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_decode(p, a->d, a->dtype, st) != cudaSuccess) return FA_ERR_CUDA;
   if (splits_used) *splits_used = ns;
-  const int64_t o_st[3] = {a->o_strides[0], static_cast<int64_t>(a->hq) * a->d, a->o_strides[1]};
-  return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, 1, a->d, a->dtype, a->o, o_st, a->lse, stream);
+  return FA_OK;  // the decode kernel merges the splits itself
 }
 
 size_t fa_kvcache_workspace_size(const fa_kvcache_args* a, int32_t num_splits) {
@@ -636,7 +658,7 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* a, int32_t num_splits) {
   if (num_splits == 0 && !device_info(&di)) return 0;
   const int ns = num_splits > 0 ? num_splits : kvcache_splits(a, 0, di);
   const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
-  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float));
+  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float)) + counters_bytes(a->b, a->hq);
 }
 
 fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {

@@ -594,10 +594,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = hf * (BM / 2) + eg * 32;  // warpgroup eg takes chunk eg of each half
         uint32_t pp[16], pd[16];
-#pragma unroll
         // the mask only where an edge cuts this chunk; pairs of columns in packed f32x2 math
         const bool edge = cmin > c0 || cmax < c0 + 31;
         const float2 sl2v = make_float2(sl2, sl2);
+#pragma unroll
         for (int i = 0; i < 32; i += 4) {
           // L2 and D of four query rows at once (the same address in every lane)
           const float4 l4 = *reinterpret_cast<const float4*>(l2v + c0 + i);

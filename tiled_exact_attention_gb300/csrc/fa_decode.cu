@@ -8,8 +8,12 @@
 //  * 7.1-7.2: the KV range is cut into num_splits contiguous block ranges, one
 //    CTA each, so that the grid fills the GPU;
 //  * 7.3: each split writes its normalised partial output and its LSE (-inf for
-//    a split with no visible key) and the combine kernel merges them with
-//    weights e^(LSE_s - LSE).
+//    a split with no visible key); the partials are merged with weights
+//    e^(LSE_s - LSE).  Here the merge is fused into the split kernel: the last
+//    CTA of a (batch, head group) to finish, found with one atomic counter per
+//    group, merges all splits' partials (still in L2) into O and LSE, so no
+//    second launch waits on the tail of the first.  fa_combine_kernel keeps the
+//    same merge as a kernel of its own for the multi-row split path.
 // K/V blocks stream through a shared-memory ring filled by TMA; eight compute
 // warps each take 8 rows of every block and keep their own running (m, l, o)
 // per head (packed f32x2 FMAs), merged across warps at the end of the split.
@@ -23,14 +27,18 @@ namespace fa {
 namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr int kDecBN = 64;          // keys per stage
 constexpr int kDecWarps = 8;        // compute warps
-constexpr int kDecRowsPerWarp = kDecBN / kDecWarps;
+constexpr int kDecSubRows = 64;     // rows of the smallest TMA box (a 64-key page)
 
 template <int D>
 struct DecCfg {
-  static constexpr int STAGES = (D == 256) ? 2 : 4;
-  static constexpr int KV_BYTES = kDecBN * D * 2;        // one K or V block
+  // keys per ring stage: the larger the TMA boxes, the closer the stream gets to
+  // the copy bandwidth (128-key stages measured 10% faster than 64-key ones at
+  // d = 128); d = 256 keeps 64 so that three stages still fit
+  static constexpr int BN = (D == 256) ? 64 : 128;
+  static constexpr int STAGES = (D == 256) ? 3 : (D == 128) ? 3 : 6;
+  static constexpr int ROWS_PER_WARP = BN / kDecWarps;
+  static constexpr int KV_BYTES = BN * D * 2;            // one K or V block
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   // two compute warpgroups + one control warpgroup (producer and three idle
   // warps) so that registers can move to the compute warps: launched at 168 per
@@ -49,7 +57,7 @@ struct DecLane {
   static constexpr int SEG = DPL / 8;             // 16-byte segments per lane
   static constexpr int LPR = D / DPL;             // lanes per key row
   static constexpr int RPP = 32 / LPR;            // key rows per pass
-  static constexpr int PASSES = kDecRowsPerWarp / RPP;
+  static constexpr int PASSES = DecCfg<D>::ROWS_PER_WARP / RPP;
   static_assert(LPR <= 32 && 32 % LPR == 0, "lane layout");
   static_assert(PASSES >= 1, "rows per warp");
 };
@@ -84,8 +92,16 @@ enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
 
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                              float* red, int warp, int lane, int split, int bi, int kvh,
+                                              float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit);
+
+// Dynamic shared memory: the K/V ring, its barriers, the cross-warp merge buffer
+// [warps][G][D + 2] and two flag words (abort, merging CTA).
+template <int D, int G>
+constexpr int dec_smem_bytes() {
+  return DecCfg<D>::STAGES * DecCfg<D>::STAGE_BYTES + 2 * DecCfg<D>::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 16 +
+         128;
+}
 
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -97,6 +113,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + C::STAGES;
   float* red = reinterpret_cast<float*>(empty + C::STAGES);  // [warps][G][D + 2]
+  int* flags = reinterpret_cast<int*>(red + kDecWarps * G * (D + 2));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, bi = blockIdx.z;
@@ -115,13 +132,13 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
     }
     limit = max(limit, 0);
     start = p.window_left >= 0 ? max(0, limit - 1 - p.window_left) : 0;
-    nblk = (limit + kDecBN - 1) / kDecBN;
+    nblk = (limit + C::BN - 1) / C::BN;
     // every sequence is cut into num_splits ranges of its own length (measured
     // better balanced than ranges of one size set by the longest sequence)
-    bps = max(1, (nblk - start / kDecBN + p.num_splits - 1) / p.num_splits);
+    bps = max(1, (nblk - start / C::BN + p.num_splits - 1) / p.num_splits);
   }
   // blocks before the sliding window's left edge are never read
-  const int blk_lo = start / kDecBN + split * bps;
+  const int blk_lo = start / C::BN + split * bps;
   const int blk_hi = min(nblk, blk_lo + bps);
   const int nb = max(0, blk_hi - blk_lo);
 
@@ -131,6 +148,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
       mbar_init(&empty[s], kDecWarps);
     }
     fence_mbar_init();
+    flags[0] = 0;
+    flags[1] = 0;
   }
   __syncthreads();
 
@@ -145,30 +164,52 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
       tma_prefetch_desc(&p.tm_v);
       const uint64_t pol = l2_policy_evict_first();
       int issued = 0;
-      // paged: the page of the next block is fetched one iteration ahead, so the
-      // table lookup overlaps the wait for a free slot
+      // A block is loaded as BN / box_rows boxes (two when 64-key pages hold a
+      // 128-key block), none straddling a page.  Paged: the pages of the next
+      // block are fetched one iteration ahead, so the table lookups overlap the
+      // wait for a free slot; a box that starts past the sequence's end (its
+      // rows are masked) reuses the block's first page, so the table is never
+      // read beyond the sequence's own entries.
+      constexpr int MAXSUB = C::BN / kDecSubRows;
+      const int nsub = C::BN / p.box_rows;
       const int* bt_row = p.block_table + static_cast<int64_t>(bi) * p.bt_stride;
-      int page_next = (p.kv_mode == kKvPaged) ? bt_row[(blk_lo * kDecBN) / p.page_size] : 0;
+      int pg_next[MAXSUB];
+#pragma unroll
+      for (int j = 0; j < MAXSUB; ++j) {
+        const int r = blk_lo * C::BN + j * p.box_rows;
+        pg_next[j] = (p.kv_mode == kKvPaged && j < nsub && r < limit) ? bt_row[r / p.page_size] : -1;
+      }
       for (int i = 0; i < nb; ++i) {
         const int slot = i % C::STAGES, use = i / C::STAGES;
-        const int row = (blk_lo + i) * kDecBN;
-        const int page = page_next;
-        if (p.kv_mode == kKvPaged && i + 1 < nb) page_next = bt_row[(row + kDecBN) / p.page_size];
+        const int row = (blk_lo + i) * C::BN;
+        int pg[MAXSUB];
+#pragma unroll
+        for (int j = 0; j < MAXSUB; ++j) {
+          pg[j] = pg_next[j];
+          const int r = row + C::BN + j * p.box_rows;
+          if (p.kv_mode == kKvPaged && i + 1 < nb) pg_next[j] = (j < nsub && r < limit) ? bt_row[r / p.page_size] : -1;
+        }
         if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.status, kSiteDecEmpty)) break;
         uint8_t* st = smem + slot * C::STAGE_BYTES;
-        // coordinates (row, outer) of this block in the K/V tensor view
-        int c_row = row, c_outer = bi;
-        if (p.kv_mode == kKvPaged) {
-          // a block never straddles a page: the page size is a multiple of the block
-          c_outer = page;
-          c_row = row % p.page_size;
-        } else if (p.kv_mode == kKvPacked) {
-          c_row = row_base + row;
-          c_outer = 0;
-        }
         mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
-        tma_load_4d_hint(st, &p.tm_k, &full[slot], 0, kvh, c_row, c_outer, pol);
-        tma_load_4d_hint(st + C::KV_BYTES, &p.tm_v, &full[slot], 0, kvh, c_row, c_outer, pol);
+#pragma unroll
+        for (int j = 0; j < MAXSUB; ++j) {
+          if (j < nsub) {
+            // coordinates (row, outer) of this box in the K/V tensor view
+            const int r = row + j * p.box_rows;
+            int c_row = r, c_outer = bi;
+            if (p.kv_mode == kKvPaged) {
+              c_outer = pg[j] >= 0 ? pg[j] : pg[0];
+              c_row = r % p.page_size;
+            } else if (p.kv_mode == kKvPacked) {
+              c_row = row_base + r;
+              c_outer = 0;
+            }
+            const int off = j * p.box_rows * D * 2;
+            tma_load_4d_hint(st + off, &p.tm_k, &full[slot], 0, kvh, c_row, c_outer, pol);
+            tma_load_4d_hint(st + C::KV_BYTES + off, &p.tm_v, &full[slot], 0, kvh, c_row, c_outer, pol);
+          }
+        }
         ++issued;
       }
       for (int i = max(0, issued - C::STAGES); i < issued; ++i)
@@ -180,14 +221,66 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
     // ------------------------------ compute warps ------------------------------
     // (each register budget covers only its own role's code)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_COMPUTE));
-    compute_split<D, G, BF16>(p, smem, full, empty, red, warp, lane, split, bi, kvh, h_first, blk_lo, nb, start,
-                              limit);
+    compute_split<D, G, BF16>(p, smem, full, empty, red, flags, warp, lane, split, bi, kvh, h_first, blk_lo, nb,
+                              start, limit);
+  }
+}
+
+// The merge of all splits of one (batch, head group), run by the CTA that
+// finished last (its 256 compute threads): per head h, LSE = logsumexp_s LSE_s
+// and weights w_s = e^(LSE_s - LSE) (0 for a split that saw no key) into
+// shared memory, then O = sum_s w_s O_s per dim; a head whose splits all saw no
+// key gets O = 0 and LSE = -inf.  The partials are read through L2 (__ldcg):
+// other SMs wrote them.
+template <int D, int G, bool BF16>
+__device__ __forceinline__ void merge_splits(const DecodeParams& p, float* wts, int bi, int h_first) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ns = p.num_splits;
+  const int64_t nrows = static_cast<int64_t>(p.b) * p.hq;  // partial rows per split (sq == 1)
+  if (warp < G) {
+    const int64_t row = static_cast<int64_t>(bi) * p.hq + h_first + warp;
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(p.lse_part + s * nrows + row));
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    float lse = -INFINITY;
+    if (M != -INFINITY) {
+      float ssum = 0.f;
+      for (int s = lane; s < ns; s += 32) ssum += ex2_approx((__ldcg(p.lse_part + s * nrows + row) - M) * kLog2e);
+#pragma unroll
+      for (int x = 16; x > 0; x >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, x);
+      lse = M + lg2_approx(ssum) * kLn2;
+    }
+    for (int s = lane; s < ns; s += 32) {
+      const float ls = __ldcg(p.lse_part + s * nrows + row);
+      wts[warp * ns + s] = (ls == -INFINITY) ? 0.f : ex2_approx((ls - lse) * kLog2e);
+    }
+    if (lane == 0 && p.lse != nullptr) p.lse[row] = lse;
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  for (int idx = threadIdx.x; idx < G * D; idx += kDecWarps * 32) {
+    const int h = idx / D, e = idx % D;
+    const int64_t row = static_cast<int64_t>(bi) * p.hq + h_first + h;
+    const float* op = p.o_part + row * D + e;
+    float o = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < ns; ++s) {
+      const float w = wts[h * ns + s];
+      if (w != 0.f) o = fmaf(w, __ldcg(op + s * nrows * D), o);
+    }
+    uint16_t* orow = static_cast<uint16_t*>(p.o) + bi * p.o_stride_b + (h_first + h) * p.o_stride_h;
+    if constexpr (BF16) {
+      orow[e] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    } else {
+      orow[e] = __half_as_ushort(__float2half_rn(o));
+    }
   }
 }
 
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                              float* red, int warp, int lane, int split, int bi, int kvh,
+                                              float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit) {
   using C = DecCfg<D>;
   using L = DecLane<D, G>;
@@ -222,18 +315,18 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     }
     const uint8_t* ks = smem + slot * C::STAGE_BYTES;
     const uint8_t* vs = ks + C::KV_BYTES;
-    const int key0 = (blk_lo + i) * kDecBN + warp * kDecRowsPerWarp;
+    const int key0 = (blk_lo + i) * C::BN + warp * C::ROWS_PER_WARP;
     // the last block of a sequence may hold rows past its end (another sequence's
     // keys, or cache slots never written), the first one rows before the window:
     // their V rows are zeroed below
-    const bool edge_block = (blk_lo + i + 1) * kDecBN > limit || (blk_lo + i) * kDecBN < start;
+    const bool edge_block = (blk_lo + i + 1) * C::BN > limit || (blk_lo + i) * C::BN < start;
     if (edge_block) {
       // zero this warp's V rows outside [start, limit) in shared memory (the TMA
       // copy has landed: the full barrier was waited on), so the loop below stays as is
       uint8_t* vw = smem + slot * C::STAGE_BYTES + C::KV_BYTES;
 #pragma unroll
       for (int ps = 0; ps < L::PASSES; ++ps) {
-        const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+        const int kr = warp * C::ROWS_PER_WARP + ps * L::RPP + rg;
         const int key = key0 + ps * L::RPP + rg;
         if (key >= limit || key < start) {
 #pragma unroll
@@ -247,7 +340,7 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     float sc[L::PASSES][G];
 #pragma unroll
     for (int ps = 0; ps < L::PASSES; ++ps) {
-      const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+      const int kr = warp * C::ROWS_PER_WARP + ps * L::RPP + rg;
       float kf[L::DPL];
 #pragma unroll
       for (int s = 0; s < L::SEG; ++s) {
@@ -301,7 +394,7 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     }
 #pragma unroll
     for (int ps = 0; ps < L::PASSES; ++ps) {
-      const int kr = warp * kDecRowsPerWarp + ps * L::RPP + rg;
+      const int kr = warp * C::ROWS_PER_WARP + ps * L::RPP + rg;
       float vf[L::DPL];
 #pragma unroll
       for (int s = 0; s < L::SEG; ++s) {
@@ -355,9 +448,10 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
       }
     }
   }
+  if (!ok) flags[0] = 1;  // a wait gave up: no partial is written and nothing merged
   // all compute threads (and the producer) meet here
   __syncthreads();
-  if (!ok) return;
+  if (flags[0] != 0) return;
   const int nthreads = kDecWarps * 32;
   for (int idx = threadIdx.x; idx < G * D; idx += nthreads) {
     const int h = idx / D, e = idx % D;
@@ -378,13 +472,25 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     p.o_part[prow * D + e] = Lsum > 0.f ? o / Lsum : 0.f;
     if (e == 0) p.lse_part[prow] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
   }
+  // ---- fused merge: the last CTA of this (batch, group) to count itself in ----
+  __threadfence();  // this CTA's partials are visible device-wide before it counts itself
+  named_bar_sync(1, kDecWarps * 32);
+  const int64_t ctr = static_cast<int64_t>(bi) * gridDim.y + blockIdx.y;
+  if (threadIdx.x == 0) flags[1] = atomicAdd(p.counters + ctr, 1) == p.num_splits - 1;
+  named_bar_sync(1, kDecWarps * 32);
+  if (flags[1] == 0) return;
+  __threadfence();
+  // the K/V ring is idle now (every block consumed, the producer drained): it
+  // holds the merge weights
+  merge_splits<D, G, BF16>(p, reinterpret_cast<float*>(smem), bi, h_first);
+  if (threadIdx.x == 0) p.counters[ctr] = 0;
 }
 
 template <int D, int G, bool BF16>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
   auto kern = fa_decode_kernel<D, G, BF16>;
-  const int smem = C::STAGES * C::STAGE_BYTES + 2 * C::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 128;
+  const int smem = dec_smem_bytes<D, G>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.hkv * (p.g / G), p.b);
@@ -395,7 +501,7 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
 template <int D, int G, bool BF16>
 int dec_occupancy() {
   using C = DecCfg<D>;
-  const int smem = C::STAGES * C::STAGE_BYTES + 2 * C::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 128;
+  const int smem = dec_smem_bytes<D, G>();
   auto kern = fa_decode_kernel<D, G, BF16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
   int n = 0;
@@ -485,7 +591,13 @@ __global__ void fa_wait_selftest_kernel(int* status) {
 
 }  // namespace
 
-int decode_block_n(int) { return kDecBN; }
+int decode_block_n(int d) {
+  switch (d) {
+    case 64: return DecCfg<64>::BN;
+    case 128: return DecCfg<128>::BN;
+    default: return DecCfg<256>::BN;
+  }
+}
 
 int decode_heads_per_cta(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1; }
 

@@ -72,9 +72,17 @@ struct DecodeParams {
   int kv_mode;                  // kKvDense, kKvPaged or kKvPacked
   const int* block_table;       // paged: [b][bt_stride] page indices
   int64_t bt_stride;
-  int page_size;                // paged: keys per page, multiple of the 64-key block
+  int page_size;                // paged: keys per page, a multiple of 64
+  int box_rows;                 // rows per TMA box: the key block, or 64 when pages are smaller than it
   const int* seqlens;           // paged: [b] keys per sequence
   const int* cu_seqlens;        // packed: [b + 1] prefix sums of keys per sequence
+  // Fused merge: the last split of a (batch, query-head group) to finish merges
+  // all splits' partials into o / lse.  counters: one int per (batch, group),
+  // zero at launch; the merging CTA puts its counter back to zero.
+  int* counters;                // [b][hkv * g / heads_per_cta]
+  void* o;                      // [b][1][hq][d] of the input type
+  int64_t o_stride_b, o_stride_h;
+  float* lse;                   // [b][hq], or null
 };
 
 // Parameters of the backward kernels (recompute form: D and log2-scaled LSE per
