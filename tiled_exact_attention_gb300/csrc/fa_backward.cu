@@ -61,24 +61,26 @@ struct BwdCfg {
   static_assert(EW_THREADS * REG_EW + 128 * REG_CONTROL <= THREADS * 168, "register split");
   static constexpr int TMEM_COLS = 512;
   // dQ kernel: Q and dO tiles, then a ring of K / V blocks
-  static constexpr int DQ_STAGES = 4;
+  static constexpr int DQ_STAGES = 5;
   static constexpr int DQ_RING_OFF = 2 * TILE_BYTES;
   static constexpr int DQ_BAR_OFF = DQ_RING_OFF + DQ_STAGES * TILE_BYTES;
   // (at least 117 KiB, so that one CTA, which holds all 512 TMEM columns, runs per SM)
   static constexpr int MIN_SMEM = 117 * 1024;
-  static constexpr int DQ_SMEM_RAW = DQ_BAR_OFF + 8 * (1 + 2 * DQ_STAGES + 4) + 16 + 1024;
+  static constexpr int DQ_SMEM_RAW = DQ_BAR_OFF + 8 * (2 * DQ_STAGES + 7) + 16 + 1024;
   static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
   // dK / dV kernel: K and V tiles, then stages of (Q tile, dO tile, L and D of their rows)
   static constexpr int KV_STAGES = 2;
   static constexpr int QD_STAGE_BYTES = 2 * TILE_BYTES + 1024;  // + 128 floats of L, 128 of D
   static constexpr int QD_OFF = 2 * TILE_BYTES;
   static constexpr int KV_BAR_OFF = QD_OFF + KV_STAGES * QD_STAGE_BYTES;
-  static constexpr int KV_SMEM_RAW = KV_BAR_OFF + 8 * (1 + 2 * KV_STAGES + 4) + 16 + 1024;
+  static constexpr int KV_SMEM_RAW = KV_BAR_OFF + 8 * (2 * KV_STAGES + 8) + 16 + 1024;
   static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
   static_assert(DQ_SMEM <= 227 * 1024 && KV_SMEM <= 227 * 1024, "shared memory budget");
   static_assert(QD_STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  // TMEM: S (or S^T) at 0, dP (or dP^T) at 128, accumulators from 256
-  static constexpr int S_COL = 0, DP_COL = 128, ACC_COL = 256;
+  // TMEM: S (or S^T) at 0, dP (or dP^T) at 128, accumulators from 256; the dQ
+  // kernel keeps a second S buffer at 384 (S of the next block while dQ reads dS)
+  static constexpr int S_COL = 0, DP_COL = 128, ACC_COL = 256, S2_COL = 384;
+  static_assert(ACC_COL + D <= S2_COL, "the dQ accumulator and the second S buffer must not overlap");
   static_assert(ACC_COL + 2 * D <= TMEM_COLS, "dK and dV accumulators must fit in TMEM");
 };
 
@@ -205,8 +207,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::DQ_BAR_OFF);  // Q and dO landed
   uint64_t* kv_full = q_full + 1;
   uint64_t* kv_empty = kv_full + ST;
-  uint64_t* s_full = kv_empty + ST;   // S and dP of a block are in TMEM
-  uint64_t* ds_half = s_full + 1;     // dS of the first / second half of a block's keys is in TMEM
+  uint64_t* s_full = kv_empty + ST;   // S of a block is in TMEM, one barrier per S buffer
+  uint64_t* dp_full = s_full + 2;     // dP of a block is in TMEM
+  uint64_t* ds_half = dp_full + 1;    // dS of the first / second half of a block's keys is in TMEM
   uint64_t* dq_done = ds_half + 2;    // every dQ MMA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_done + 1);
 
@@ -222,7 +225,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(dp_full, 1);
     mbar_init(&ds_half[0], C::EW_THREADS);
     mbar_init(&ds_half[1], C::EW_THREADS);
     mbar_init(dq_done, 1);
@@ -279,37 +284,57 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::TILE_BYTES), 16, 1024);
       const uint64_t kk_desc = sdesc_sw128(ring_s, 16, 1024);        // a ring slot read K-major
       const uint64_t kmn_desc = sdesc_sw128(ring_s, BN * 128, 1024);  // a ring slot read MN-major
-      bool ok = mbar_wait(q_full, 0, p.status, kSiteBwdQFull);
-      for (int it = 0; ok && it < N; ++it) {
-        const int Lk = 2 * it, Lv = 2 * it + 1;
-        if (!mbar_wait(&kv_full[Lk % ST], (Lk / ST) & 1, p.status, kSiteBwdKvFull) ||
-            !mbar_wait(&kv_full[Lv % ST], (Lv / ST) & 1, p.status, kSiteBwdKvFull))
-          break;
+      // Software-pipelined over the key blocks: S of block it + 1 goes to the other
+      // S buffer at the start of iteration it, and dP of block it + 1 as soon as the
+      // elementwise warps are done with block it, so they form P of the next block
+      // while the tensor pipe runs dQ of this one (in issue order).  Every barrier
+      // is at most one phase ahead of its waiters: S of block it + 2 is issued only
+      // after block it (the same S buffer and barrier) is done.
+#define FA_SCOL(i) ((i) & 1 ? C::S2_COL : C::S_COL)
+      bool ok = mbar_wait(q_full, 0, p.status, kSiteBwdQFull) &&
+                mbar_wait(&kv_full[0], 0, p.status, kSiteBwdKvFull) && mbar_wait(&kv_full[1], 0, p.status, kSiteBwdKvFull);
+      if (ok) {
         tc_fence_after();
-        // S = Q K^T and dP = dO V^T (the previous dQ MMA has read the dS columns: in order)
-        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, q_desc, kk_desc, 0, Lk % ST);
-        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0,
-                                                                    Lv % ST);
-        umma_commit(s_full);
-        umma_commit(&kv_empty[Lv % ST]);
-        // dQ += dS K, half a block of keys at a time (the products of the first half run
-        // while the second half is formed): dS of keys [32 c, 32 c + 32) is packed at S
-        // columns [32 c, 32 c + 16), the first columns of the chunk its warp has read;
-        // K is read MN-major
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, q_desc, kk_desc, 0, 0);
+        umma_commit(&s_full[0]);
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0, 1);
+        umma_commit(dp_full);
+        umma_commit(&kv_empty[1]);
+      }
+      for (int it = 0; ok && it < N; ++it) {
+        const int Lk = 2 * it, Lk1 = 2 * it + 2, Lv1 = 2 * it + 3;
+        const bool more = it + 1 < N;
+        // S of the next block into the other buffer (dQ of block it - 1 has read it: in order)
+        if (more) {
+          if (!mbar_wait(&kv_full[Lk1 % ST], (Lk1 / ST) & 1, p.status, kSiteBwdKvFull)) break;
+          tc_fence_after();
+          issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + FA_SCOL(it + 1), q_desc, kk_desc, 0,
+                                                                      Lk1 % ST);
+          umma_commit(&s_full[(it + 1) & 1]);
+        }
+        // dQ += dS K by halves of the block's keys: dS of keys [32 c, 32 c + 32) is packed
+        // at columns [32 c, 32 c + 16) of the block's S buffer; K is read MN-major
         if (!mbar_wait(&ds_half[0], it & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, 2>(tbase + C::ACC_COL, tbase + C::S_COL, kmn_desc, Lk % ST,
-                                                        it > 0);
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 2, 4>(tbase + C::ACC_COL, tbase + C::S_COL + 16, kmn_desc,
-                                                        Lk % ST, true);
+        const uint32_t sc = tbase + FA_SCOL(it);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 0, 2>(tbase + C::ACC_COL, sc, kmn_desc, Lk % ST, it > 0);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 2, 4>(tbase + C::ACC_COL, sc + 16, kmn_desc, Lk % ST, true);
         if (!mbar_wait(&ds_half[1], it & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 4, 6>(tbase + C::ACC_COL, tbase + C::S_COL + 32, kmn_desc,
-                                                        Lk % ST, true);
-        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 6, 8>(tbase + C::ACC_COL, tbase + C::S_COL + 48, kmn_desc,
-                                                        Lk % ST, true);
+        // the elementwise warps are done with block it (and have read its dP): the next block's dP
+        if (more) {
+          if (!mbar_wait(&kv_full[Lv1 % ST], (Lv1 / ST) & 1, p.status, kSiteBwdKvFull)) break;
+          tc_fence_after();
+          issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0,
+                                                                      Lv1 % ST);
+          umma_commit(dp_full);
+          umma_commit(&kv_empty[Lv1 % ST]);
+        }
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 4, 6>(tbase + C::ACC_COL, sc + 32, kmn_desc, Lk % ST, true);
+        issue_pv_tile<D, BN, C::TILE_BYTES, kIdQ, 6, 8>(tbase + C::ACC_COL, sc + 48, kmn_desc, Lk % ST, true);
         umma_commit(&kv_empty[Lk % ST]);
       }
+#undef FA_SCOL
       umma_commit(dq_done);
       mbar_wait(dq_done, 0, p.status, kSiteBwdDrain, true);
     }
@@ -322,7 +347,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
     const int r = 32 * (warp & 3) + lane;
     const int row = row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tbase + lane_off + C::S_COL;
     const uint32_t tP = tbase + lane_off + C::DP_COL;
     const int64_t prow = (static_cast<int64_t>(bi) * p.hq + h) * p.sq_pad + row;  // row < sq_pad
     const float l2 = p.l2pre[prow];
@@ -334,38 +358,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
     bool ok = true;
     for (int it = 0; it < N; ++it) {
       const int n = n_hi - 1 - it;
-      if (!warp_wait(s_full, it & 1, p.status, kSiteBwdSFull)) {
+      const uint32_t tSb = tbase + lane_off + ((it & 1) ? C::S2_COL : C::S_COL);  // this block's S buffer
+      // ---- P = 2^(S scale log2 e - L2) as soon as S is in TMEM ----
+      if (!warp_wait(&s_full[it & 1], (it >> 1) & 1, p.status, kSiteBwdSFull)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int lim = lim_row - n * BN, lo = lo_row - n * BN;
       // chunk of 32 keys: warpgroup eg takes chunk eg of each half; the half is
-      // signalled once both warpgroups have packed their chunk
-      // both chunks of this warpgroup loaded at once (the second load's latency hides
-      // behind the first chunk's arithmetic)
-      uint32_t sv2[2][32], pv2[2][32];
+      // signalled once both warpgroups have packed their chunk; both chunks of this
+      // warpgroup are loaded at once (the second load's latency hides behind the
+      // first chunk's arithmetic)
+      uint32_t sv2[2][32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        tmem_ld32_issue(tS + hf * (BN / 2) + eg * 32, sv2[hf]);
-        tmem_ld32_issue(tP + hf * (BN / 2) + eg * 32, pv2[hf]);
-      }
+      for (int hf = 0; hf < 2; ++hf) tmem_ld32_issue(tSb + hf * (BN / 2) + eg * 32, sv2[hf]);
       tmem_ld_wait();
       reg_fence<32>(sv2[0]);
       reg_fence<32>(sv2[1]);
-      reg_fence<32>(pv2[0]);
-      reg_fence<32>(pv2[1]);
+      float pf[2][32];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = hf * (BN / 2) + eg * 32;
-        const uint32_t* sv = sv2[hf];
-        const uint32_t* pv = pv2[hf];
         const bool edge = lim < c0 + 32 || lo > c0;
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           // pairs of keys in packed f32x2 math; the mask only where an edge cuts the chunk
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv2[hf][i]), __uint_as_float(sv2[hf][i + 1])),
                                       make_float2(sl2, sl2), make_float2(-l2, -l2));
           float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (edge) {
@@ -373,11 +392,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
             if (c >= lim || c < lo) pr.x = 0.f;
             if (c + 1 >= lim || c + 1 < lo) pr.y = 0.f;
           }
-          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
-                                                      make_float2(-dd, -dd)));
+          pf[hf][i] = pr.x;
+          pf[hf][i + 1] = pr.y;
+        }
+      }
+      // ---- dS = P (dP - D) once dP is in TMEM ----
+      if (!warp_wait(dp_full, it & 1, p.status, kSiteBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pv2[2][32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) tmem_ld32_issue(tP + hf * (BN / 2) + eg * 32, pv2[hf]);
+      tmem_ld_wait();
+      reg_fence<32>(pv2[0]);
+      reg_fence<32>(pv2[1]);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = hf * (BN / 2) + eg * 32;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 ds = __fmul2_rn(make_float2(pf[hf][i], pf[hf][i + 1]),
+                                       __fadd2_rn(make_float2(__uint_as_float(pv2[hf][i]), __uint_as_float(pv2[hf][i + 1])),
+                                                  make_float2(-dd, -dd)));
           pk[i / 2] = pack2<BF16>(ds.x, ds.y);
         }
-        tmem_st16(tS + c0, pk);
+        tmem_st16(tSb + c0, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&ds_half[hf]);
@@ -428,9 +470,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + C::KV_BAR_OFF);  // K and V landed
   uint64_t* qd_full = kv_full + 1;   // per stage: Q, dO, L2, D of a query tile landed
   uint64_t* qd_empty = qd_full + ST;
-  uint64_t* s_full = qd_empty + ST;  // S^T and dP^T in TMEM
-  uint64_t* p_half = s_full + 1;     // P^T and dS^T of the first / second half of a tile's rows in TMEM
-  uint64_t* mma_done = p_half + 2;
+  uint64_t* s_full = qd_empty + ST;  // S^T in TMEM
+  uint64_t* dp_full = s_full + 1;    // dP^T in TMEM
+  uint64_t* p_half = dp_full + 1;    // P^T of the first / second half of a tile's rows in TMEM
+  uint64_t* ds_half = p_half + 2;    // dS^T of the first / second half
+  uint64_t* mma_done = ds_half + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   auto stage_ptr = [&](int s) { return smem + C::QD_OFF + s * C::QD_STAGE_BYTES; };
 
@@ -447,8 +491,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(&p_half[0], C::EW_THREADS);
-    mbar_init(&p_half[1], C::EW_THREADS);
+    mbar_init(dp_full, 1);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(&p_half[hf], C::EW_THREADS);
+      mbar_init(&ds_half[hf], C::EW_THREADS);
+    }
     mbar_init(mma_done, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&qd_full[s], 1);
@@ -502,34 +549,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
     if (lane == 0 && T > 0) {
       constexpr uint32_t kIdS = idesc_f16(BN, BM, BF16, false);  // S^T: M = keys, N = query rows
       constexpr uint32_t kIdA = idesc_f16(BN, D, BF16, true);    // dV, dK: M = keys, N = d, B MN-major
-      const uint64_t k_desc = sdesc_sw128(smem_u32(smem), 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::TILE_BYTES), 16, 1024);
-      bool ok = mbar_wait(kv_full, 0, p.status, kSiteBwdKvFull);
-      for (int ti = 0; ok && ti < T; ++ti) {
-        const int s = ti % ST;
-        if (!mbar_wait(&qd_full[s], (ti / ST) & 1, p.status, kSiteBwdQdFull)) break;
+      const uint32_t k_s = smem_u32(smem);  // K tile, then V tile (read K-major)
+      // (descriptors are formed where they are used: fewer live registers in this warp)
+#define FA_KDESC() sdesc_sw128(opaque_u32(k_s), 16, 1024)
+#define FA_VDESC() sdesc_sw128(opaque_u32(k_s) + C::TILE_BYTES, 16, 1024)
+      // Software-pipelined over the query tiles: the next tile's S^T is issued as
+      // soon as dV has read this tile's P^T out of its columns, and its dP^T as soon
+      // as dK has read dS^T, so the elementwise warps form P of tile ti + 1 while
+      // the tensor pipe still runs dK of tile ti (the pipe executes in issue order).
+      bool ok = mbar_wait(kv_full, 0, p.status, kSiteBwdKvFull) && mbar_wait(&qd_full[0], 0, p.status, kSiteBwdQdFull);
+      if (ok) {
         tc_fence_after();
+        const uint32_t st0 = smem_u32(stage_ptr(0));
+        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, FA_KDESC(), sdesc_sw128(st0, 16, 1024),
+                                                                    0, 0);
+        umma_commit(s_full);
+        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, FA_VDESC(),
+                                                                    sdesc_sw128(st0 + C::TILE_BYTES, 16, 1024), 0, 0);
+        umma_commit(dp_full);
+      }
+      for (int ti = 0; ok && ti < T; ++ti) {
+        const int s = ti % ST, s1 = (ti + 1) % ST;
+        const bool more = ti + 1 < T;
         const uint32_t st = smem_u32(stage_ptr(s));
-        const uint64_t qk_desc = sdesc_sw128(st, 16, 1024);                            // Q, K-major
-        const uint64_t dok_desc = sdesc_sw128(st + C::TILE_BYTES, 16, 1024);          // dO, K-major
         const uint64_t qmn_desc = sdesc_sw128(st, BM * 128, 1024);                     // Q, MN-major
         const uint64_t domn_desc = sdesc_sw128(st + C::TILE_BYTES, BM * 128, 1024);  // dO, MN-major
-        // S^T = K Q^T, dP^T = V dO^T (the previous dV / dK MMAs have read these columns: in order)
-        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, k_desc, qk_desc, 0, 0);
-        issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, v_desc, dok_desc, 0, 0);
-        umma_commit(s_full);
-        // dV += P^T dO, dK += dS^T Q, half a tile of query rows at a time (the products
-        // of the first half run while the second half is formed); P^T / dS^T of rows
-        // [32 c, 32 c + 32) are packed at columns [32 c, 32 c + 16) of their region;
-        // dO and Q are read MN-major
+        // dV += P^T dO, half a tile of query rows at a time (the first half's products
+        // run while the second half is formed); P^T of rows [32 c, 32 c + 32) is packed
+        // at columns [32 c, 32 c + 16) of the S^T region, dO is read MN-major
         if (!mbar_wait(&p_half[0], ti & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, 2>(tbase + C::ACC_COL, tbase + C::S_COL, domn_desc, 0, ti > 0);
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 2, 4>(tbase + C::ACC_COL, tbase + C::S_COL + 16, domn_desc, 0,
-                                                        true);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, 2>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
-                                                        ti > 0);
-        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 2, 4>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 16, qmn_desc, 0,
                                                         true);
         if (!mbar_wait(&p_half[1], ti & 1, p.status, kSiteBwdDsFull)) break;
         tc_fence_after();
@@ -537,12 +588,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
                                                         true);
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 6, 8>(tbase + C::ACC_COL, tbase + C::S_COL + 48, domn_desc, 0,
                                                         true);
+        // the next tile's S^T = K Q^T over the columns dV has just read
+        if (more) {
+          if (!mbar_wait(&qd_full[s1], ((ti + 1) / ST) & 1, p.status, kSiteBwdQdFull)) break;
+          tc_fence_after();
+          issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(
+              tbase + C::S_COL, FA_KDESC(), sdesc_sw128(opaque_u32(smem_u32(stage_ptr(s1))), 16, 1024), 0, 0);
+          umma_commit(s_full);
+        }
+        // dK += dS^T Q, likewise by halves; Q read MN-major
+        if (!mbar_wait(&ds_half[0], ti & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 0, 2>(tbase + C::ACC_COL + D, tbase + C::DP_COL, qmn_desc, 0,
+                                                        ti > 0);
+        issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 2, 4>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 16, qmn_desc, 0,
+                                                        true);
+        if (!mbar_wait(&ds_half[1], ti & 1, p.status, kSiteBwdDsFull)) break;
+        tc_fence_after();
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 4, 6>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 32, qmn_desc, 0,
                                                         true);
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 6, 8>(tbase + C::ACC_COL + D, tbase + C::DP_COL + 48, qmn_desc, 0,
                                                         true);
+        // the next tile's dP^T = V dO^T over the columns dK has just read
+        if (more) {
+          issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(
+              tbase + C::DP_COL, FA_VDESC(), sdesc_sw128(opaque_u32(smem_u32(stage_ptr(s1))) + C::TILE_BYTES, 16, 1024),
+              0, 0);
+          umma_commit(dp_full);
+        }
         umma_commit(&qd_empty[s]);
       }
+#undef FA_KDESC
+#undef FA_VDESC
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, p.status, kSiteBwdDrain, true);
     }
@@ -562,7 +639,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
     for (int ti = 0; ti < T; ++ti) {
       const int s = ti % ST;
       const int m = m_lo + ti % nm;
-      // the L2 and D vectors were written by the copy engine: observe their arrival
+      // ---- P^T = 2^(S^T scale log2 e - L2) as soon as S^T is in TMEM ----
+      // (the L2 and D vectors were written by the copy engine: observe their arrival)
       if (!warp_wait(&qd_full[s], (ti / ST) & 1, p.status, kSiteBwdQdFull) ||
           !warp_wait(s_full, ti & 1, p.status, kSiteBwdSFull)) {
         ok = false;
@@ -579,33 +657,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       if (p.local) cmax = min(cmax, j - p.left_off - i0);    // j >= i + left_off
       // both chunks of this warpgroup (one per half) are loaded at once, so the
       // second load's latency hides behind the first chunk's arithmetic
-      uint32_t sv[2][32], pv[2][32];
+      uint32_t sv[2][32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        tmem_ld32_issue(tS + hf * (BM / 2) + eg * 32, sv[hf]);
-        tmem_ld32_issue(tP + hf * (BM / 2) + eg * 32, pv[hf]);
-      }
+      for (int hf = 0; hf < 2; ++hf) tmem_ld32_issue(tS + hf * (BM / 2) + eg * 32, sv[hf]);
       tmem_ld_wait();
       reg_fence<32>(sv[0]);
       reg_fence<32>(sv[1]);
-      reg_fence<32>(pv[0]);
-      reg_fence<32>(pv[1]);
+      float pf[2][32];  // P in fp32, kept for dS
+      const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = hf * (BM / 2) + eg * 32;  // warpgroup eg takes chunk eg of each half
-        uint32_t pp[16], pd[16];
         // the mask only where an edge cuts this chunk; pairs of columns in packed f32x2 math
         const bool edge = cmin > c0 || cmax < c0 + 31;
-        const float2 sl2v = make_float2(sl2, sl2);
+        uint32_t pp[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          // L2 and D of four query rows at once (the same address in every lane)
+          // L2 of four query rows at once (the same address in every lane)
           const float4 l4 = *reinterpret_cast<const float4*>(l2v + c0 + i);
-          const float4 d4 = *reinterpret_cast<const float4*>(dv + c0 + i);
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const float2 nl = e == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
-            const float2 nd = e == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[hf][i + e]), __uint_as_float(sv[hf][i + e + 1])),
                                         sl2v, nl);
             float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -614,17 +686,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
               if (c < cmin || c > cmax) pr.x = 0.f;
               if (c + 1 < cmin || c + 1 > cmax) pr.y = 0.f;
             }
-            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(pv[hf][i + e]), __uint_as_float(pv[hf][i + e + 1])), nd);
-            const float2 ds = __fmul2_rn(pr, dpd);
+            pf[hf][i + e] = pr.x;
+            pf[hf][i + e + 1] = pr.y;
             pp[(i + e) / 2] = pack2<BF16>(pr.x, pr.y);
-            pd[(i + e) / 2] = pack2<BF16>(ds.x, ds.y);
           }
         }
         tmem_st16(tS + c0, pp);
-        tmem_st16(tP + c0, pd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_half[hf]);
+      }
+      // ---- dS^T = P^T (dP^T - D) once dP^T is in TMEM ----
+      if (!warp_wait(dp_full, ti & 1, p.status, kSiteBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pv[2][32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) tmem_ld32_issue(tP + hf * (BM / 2) + eg * 32, pv[hf]);
+      tmem_ld_wait();
+      reg_fence<32>(pv[0]);
+      reg_fence<32>(pv[1]);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = hf * (BM / 2) + eg * 32;
+        uint32_t pd[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dv + c0 + i);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const float2 nd = e == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
+            const float2 dpd = __fadd2_rn(make_float2(__uint_as_float(pv[hf][i + e]), __uint_as_float(pv[hf][i + e + 1])), nd);
+            const float2 ds = __fmul2_rn(make_float2(pf[hf][i + e], pf[hf][i + e + 1]), dpd);
+            pd[(i + e) / 2] = pack2<BF16>(ds.x, ds.y);
+          }
+        }
+        tmem_st16(tP + c0, pd);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_half[hf]);
       }
     }
     const bool valid = j < p.skv;
