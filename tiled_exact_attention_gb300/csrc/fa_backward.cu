@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
       }
       const uint64_t pol = l2_policy_evict_last();
       int issued = 0;
+      // V_j, then K_j: V is released as soon as dP has read it, K only once dQ has
+      // (it is read twice), so with V first each load reuses a slot freed earlier
       for (int L = 0; L < 2 * N; ++L) {
         const int slot = L % ST, use = L / ST;
         if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, p.status, kSiteBwdKvEmpty, false, 128)) break;
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
         mbar_arrive_expect_tx(&kv_full[slot], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::DC; ++c)
-          tma_load_4d_hint(ring + slot * C::TILE_BYTES + c * (BN * 128), (L & 1) ? &p.tm_v : &p.tm_k,
+          tma_load_4d_hint(ring + slot * C::TILE_BYTES + c * (BN * 128), (L & 1) ? &p.tm_k : &p.tm_v,
                            &kv_full[slot], c * 64, kvh, n * BN, bi, pol);
         ++issued;
       }
@@ -295,14 +297,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
                 mbar_wait(&kv_full[0], 0, p.status, kSiteBwdKvFull) && mbar_wait(&kv_full[1], 0, p.status, kSiteBwdKvFull);
       if (ok) {
         tc_fence_after();
-        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, q_desc, kk_desc, 0, 0);
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::S_COL, q_desc, kk_desc, 0, 1);
         umma_commit(&s_full[0]);
-        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0, 1);
+        issue_s_tile<D, BN, BM, C::TILE_BYTES, C::TILE_BYTES, kIdS>(tbase + C::DP_COL, do_desc, kk_desc, 0, 0);
         umma_commit(dp_full);
-        umma_commit(&kv_empty[1]);
+        umma_commit(&kv_empty[0]);
       }
       for (int it = 0; ok && it < N; ++it) {
-        const int Lk = 2 * it, Lk1 = 2 * it + 2, Lv1 = 2 * it + 3;
+        const int Lk = 2 * it + 1, Lk1 = 2 * it + 3, Lv1 = 2 * it + 2;
         const bool more = it + 1 < N;
         // S of the next block into the other buffer (dQ of block it - 1 has read it: in order)
         if (more) {
