@@ -56,10 +56,14 @@ def _dist():
 
 def _kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fa_prefill.cu", "fa_decode.cu", "ptx.cuh", "fa_internal.h", "tc_common.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "tiled_exact_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = ("fa_prefill.cu", "fa_decode.cu", "fa_backward.cu", "fa_fp8.cu", "ptx.cuh", "fa_internal.h",
+                  "tc_common.cuh")
 
 
 def _profiled_traffic(kernel: str):
@@ -330,7 +334,9 @@ def run_ours(args):
                                      "traffic": None}),
         "backward": dict(bwd, roofline={"bound": "tensor", "achieved": bwd["value"], "peak": pk, "unit": "TFLOP/s",
                                         "frac": round(bwd["value"] / pk, 4), "peak_source": f"{peak_src} sustained",
-                                        "frac_of_burst": round(bwd["value"] / pk_burst, 4), "traffic": None}),
+                                        "frac_of_burst": round(bwd["value"] / pk_burst, 4),
+                                        "traffic": _profiled_traffic("fa_bwd_dkdv_kernel"),
+                                        "traffic_kernel": "fa_bwd_dkdv_kernel (the larger of the two product kernels)"}),
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
                      "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
                      "kernel": "fa_prefill_kernel<128, bf16>",
