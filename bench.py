@@ -331,7 +331,7 @@ def run_ours(args):
         "e4m3": dict(e4m3, roofline={"bound": "tensor", "achieved": e4m3["value"],
                                      "peak": round(2 * pk, 1), "unit": "TFLOP/s", "frac": round(e4m3["value"] / (2 * pk), 4),
                                      "peak_source": f"{peak_src} bf16 sustained x 2 (the nominal fp8 : bf16 ratio)",
-                                     "traffic": None}),
+                                     "traffic": _profiled_traffic("fa_prefill_kernel_e4m3")}),
         "backward": dict(bwd, roofline={"bound": "tensor", "achieved": bwd["value"], "peak": pk, "unit": "TFLOP/s",
                                         "frac": round(bwd["value"] / pk, 4), "peak_source": f"{peak_src} sustained",
                                         "frac_of_burst": round(bwd["value"] / pk_burst, 4),
