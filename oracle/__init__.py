@@ -28,6 +28,8 @@ MUT_STRICT_CAUSAL = 4
 MUT_NO_ALPHA_ON_L = 8
 MUT_BWD_NO_D = 16
 MUT_BWD_NO_SCALE = 32
+MUT_CAP_BEFORE_SCALE = 128
+MUT_CAP_NO_DERIV = 256
 MUT_BWD_DK_FROM_P = 64
 
 
@@ -58,8 +60,11 @@ def _load():
         lib.oracle_attention_window.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64,
                                                 i64, ctypes.c_double, ip, i64, dp, dp, ctypes.c_int]
         lib.oracle_attention_window.restype = ctypes.c_int
+        lib.oracle_attention_ex.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64,
+                                            i64, ctypes.c_double, ctypes.c_double, ip, i64, dp, dp, ctypes.c_int]
+        lib.oracle_attention_ex.restype = ctypes.c_int
         lib.oracle_attention_tiled.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64, i64,
-                                               ctypes.c_double, ip, i64, i64, i64, dp, dp, dp, dp,
+                                               ctypes.c_double, ctypes.c_double, ip, i64, i64, i64, dp, dp, dp, dp,
                                                ctypes.c_int]
         lib.oracle_attention_tiled.restype = ctypes.c_int
         lib.oracle_combine.argtypes = [dp, dp, i64, i64, i64, dp, dp]
@@ -69,7 +74,7 @@ def _load():
         lib.oracle_visible_window.argtypes = [i64, i64, i64, ctypes.c_int, i64, i64, i64, ctypes.c_int]
         lib.oracle_visible_window.restype = ctypes.c_int
         lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, i64,
-                                             i64, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+                                             i64, ctypes.c_double, ctypes.c_double, dp, dp, dp, ctypes.c_int]
         lib.oracle_attention_bwd.restype = ctypes.c_int
         lib.oracle_split_efficiency.argtypes = [i64, i64, i64]
         lib.oracle_split_efficiency.restype = ctypes.c_double
@@ -110,10 +115,11 @@ def default_offset(sq: int, skv: int) -> int:
 
 
 def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None, scale: float | None = None,
-              rows=None, mutation: int = 0, window=(-1, -1)):
+              rows=None, mutation: int = 0, window=(-1, -1), softcap: float = 0.0):
     """Direct definition.  Returns (O [nrows, d], LSE [nrows]) for the given rows
     (default: all rows, ordered batch, head, query).  window = (left, right) widths of
-    the sliding window around key i + offset; -1 leaves a side unbounded."""
+    the sliding window around key i + offset; -1 leaves a side unbounded.  softcap = c > 0
+    caps every scaled score s to c * tanh(s / c) before the mask and the softmax."""
     lib = _load()
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     b, sq, skv, hq, hkv, d = _shapes(q, k, v)
@@ -124,9 +130,9 @@ def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None,
     o = np.zeros((n, d), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     wl, wr = (int(window[0]), int(window[1]))
-    rc = lib.oracle_attention_window(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off, wl, wr, sc,
-                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _dp(o), _dp(lse),
-                                     int(mutation))
+    rc = lib.oracle_attention_ex(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off, wl, wr, sc,
+                                 float(softcap), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _dp(o),
+                                 _dp(lse), int(mutation))
     if rc != 0:
         raise ValueError("oracle_attention: bad arguments")
     return o, lse
@@ -134,7 +140,7 @@ def attention(q, k, v, *, causal: bool = False, q_pos_offset: int | None = None,
 
 def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = False,
                     q_pos_offset: int | None = None, scale: float | None = None, rows=None, mutation: int = 0,
-                    return_partials: bool = False, window=(-1, -1)):
+                    return_partials: bool = False, window=(-1, -1), softcap: float = 0.0):
     """Tile-by-tile online-softmax model (optionally split over the key axis and merged)."""
     lib = _load()
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -148,7 +154,7 @@ def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = F
     op = np.zeros((num_splits, n, d), dtype=np.float64)
     lp = np.zeros((num_splits, n), dtype=np.float64)
     rc = lib.oracle_attention_tiled(_dp(q), _dp(k), _dp(v), b, sq, skv, hq, hkv, d, int(causal), off,
-                                    int(window[0]), int(window[1]), sc,
+                                    int(window[0]), int(window[1]), sc, float(softcap),
                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, int(tile),
                                     int(num_splits), _dp(o), _dp(lse), _dp(op), _dp(lp), int(mutation))
     if rc != 0:
@@ -159,7 +165,7 @@ def attention_tiled(q, k, v, *, tile: int, num_splits: int = 1, causal: bool = F
 
 
 def attention_bwd(q, k, v, dout, *, causal: bool = False, q_pos_offset: int | None = None,
-                  scale: float | None = None, window=(-1, -1), mutation: int = 0):
+                  scale: float | None = None, window=(-1, -1), mutation: int = 0, softcap: float = 0.0):
     """Recompute-based backward pass.  Returns (dQ like q, dK like k, dV like v) for the
     upstream gradient dout (shaped like q)."""
     lib = _load()
@@ -173,7 +179,8 @@ def attention_bwd(q, k, v, dout, *, causal: bool = False, q_pos_offset: int | No
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     rc = lib.oracle_attention_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), b, sq, skv, hq, hkv, d, int(causal), off,
-                                  int(window[0]), int(window[1]), sc, _dp(dq), _dp(dk), _dp(dv), int(mutation))
+                                  int(window[0]), int(window[1]), sc, float(softcap), _dp(dq), _dp(dk), _dp(dv),
+                                  int(mutation))
     if rc != 0:
         raise ValueError("oracle_attention_bwd: bad arguments")
     return dq, dk, dv

@@ -35,6 +35,14 @@
  *                           D = rowsum(dO * O), dS = P (dP - D), dQ = dS K * scale,
  *                           dK = dS^T Q * scale), written out row by row.
  *
+ * Softcap follows the same page's template flag Is_softcap ("a nonlinear
+ * transform of the attention scores: tanh softly limits the logits, when
+ * softcap > 0"); the page gives no formula, and the reading used here is the
+ * plainest one: each scaled score s becomes c * tanh(s / c) (c = softcap), which
+ * keeps small scores and bounds every score to (-c, c); masking, the maximum and
+ * the softmax then act on the capped scores.  In the backward pass the chain rule
+ * adds the factor dc*tanh(s/c)/ds = 1 - tanh^2(s/c) to dS.  c = 0 turns it off.
+ *
  * Sliding-window (local) attention follows "flash attention V2 code walkthrough",
  * template flag Is_local: query i sees keys in [i + skv - sq - window_left,
  * i + skv - sq + window_right], written here with the general query offset off
@@ -61,8 +69,17 @@
 #define ORACLE_MUT_NO_SCALE 2        /* both: 1/sqrt(d) (the scale) dropped          */
 #define ORACLE_MUT_STRICT_CAUSAL 4   /* both: causal j <= i + off replaced by j < ... */
 #define ORACLE_MUT_NO_ALPHA_ON_L 8   /* tiled: old denominator not rescaled by alpha */
+#define ORACLE_MUT_CAP_BEFORE_SCALE 128  /* softcap applied to the raw dot product, then scaled */
+#define ORACLE_MUT_CAP_NO_DERIV 256      /* backward: the softcap factor 1 - tanh^2 dropped */
 
-int oracle_version(void) { return 3; }
+int oracle_version(void) { return 4; }
+
+/* The score of one (query, key) pair: the scaled dot product, capped when c > 0. */
+static double capped(double dotv, double sc, double c, int mutation) {
+  if (c <= 0.0) return sc * dotv;
+  if (mutation & ORACLE_MUT_CAP_BEFORE_SCALE) return sc * (c * tanh(dotv / c));
+  return c * tanh(sc * dotv / c);
+}
 
 /* Visibility of key j to query row i; wl / wr < 0: that side of the window is unbounded. */
 int oracle_visible_window(int64_t i, int64_t j, int64_t skv, int causal, int64_t off, int64_t wl, int64_t wr,
@@ -92,9 +109,10 @@ static double dot(const double* a, const double* b, int64_t d) {
  *   o: [nrows][d], lse: [nrows].
  * Returns 0 on success, -1 on bad arguments.
  */
-int oracle_attention_window(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
-                            int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
-                            double scale, const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
+int oracle_attention_ex(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
+                        int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
+                        double scale, double softcap, const int64_t* rows, int64_t nrows, double* o, double* lse,
+                        int mutation) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0) return -1;
   const int64_t g = hq / hkv;
   const double sc = (mutation & ORACLE_MUT_NO_SCALE) ? 1.0 : scale;
@@ -122,7 +140,7 @@ int oracle_attention_window(const double* q, const double* k, const double* v, i
       int64_t nvis = 0;
       for (int64_t j = 0; j < skv; ++j) {
         if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, mutation)) continue;
-        s[j] = sc * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
+        s[j] = capped(dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d), sc, softcap, mutation);
         if (s[j] > m) m = s[j];
         ++nvis;
       }
@@ -147,11 +165,18 @@ int oracle_attention_window(const double* q, const double* k, const double* v, i
   return bad ? -1 : 0;
 }
 
+int oracle_attention_window(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
+                            int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
+                            double scale, const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
+  return oracle_attention_ex(q, k, v, b, sq, skv, hq, hkv, d, causal, off, wl, wr, scale, 0.0, rows, nrows, o, lse,
+                             mutation);
+}
+
 int oracle_attention(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
                      int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, double scale,
                      const int64_t* rows, int64_t nrows, double* o, double* lse, int mutation) {
-  return oracle_attention_window(q, k, v, b, sq, skv, hq, hkv, d, causal, off, -1, -1, scale, rows, nrows, o, lse,
-                                 mutation);
+  return oracle_attention_ex(q, k, v, b, sq, skv, hq, hkv, d, causal, off, -1, -1, scale, 0.0, rows, nrows, o, lse,
+                             mutation);
 }
 
 /*
@@ -191,7 +216,7 @@ void oracle_combine(const double* o_part, const double* lse_part, int64_t ns, in
  */
 static void one_row_tiled(const double* qrow, const double* k, const double* v, int64_t bi, int64_t i,
                           int64_t skv, int64_t hkv, int64_t kvh, int64_t d, int causal, int64_t off, int64_t wl,
-                          int64_t wr, double sc,
+                          int64_t wr, double sc, double softcap,
                           int64_t tile, int64_t t_lo, int64_t t_hi, int mutation, double* s, double* p, double* o,
                           double* lse) {
   double m = -INFINITY, l = 0.0;
@@ -203,7 +228,7 @@ static void one_row_tiled(const double* qrow, const double* k, const double* v, 
     double bmax = -INFINITY;
     for (int64_t j = j0; j < j1; ++j) {
       if (oracle_visible_window(i, j, skv, causal, off, wl, wr, mutation)) {
-        s[j - j0] = sc * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
+        s[j - j0] = capped(dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d), sc, softcap, mutation);
         if (s[j - j0] > bmax) bmax = s[j - j0];
         any = 1;
       } else {
@@ -247,8 +272,9 @@ static void one_row_tiled(const double* qrow, const double* k, const double* v, 
  */
 int oracle_attention_tiled(const double* q, const double* k, const double* v, int64_t b, int64_t sq, int64_t skv,
                            int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off, int64_t wl, int64_t wr,
-                           double scale, const int64_t* rows, int64_t nrows, int64_t tile, int64_t num_splits,
-                           double* o, double* lse, double* o_part, double* lse_part, int mutation) {
+                           double scale, double softcap, const int64_t* rows, int64_t nrows, int64_t tile,
+                           int64_t num_splits, double* o, double* lse, double* o_part, double* lse_part,
+                           int mutation) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || tile <= 0 || num_splits <= 0) return -1;
   const int64_t g = hq / hkv;
   const double sc = (mutation & ORACLE_MUT_NO_SCALE) ? 1.0 : scale;
@@ -283,8 +309,8 @@ int oracle_attention_tiled(const double* q, const double* k, const double* v, in
         int64_t t_lo = sp * nbps, t_hi = (sp + 1) * nbps;
         if (t_hi > nblk) t_hi = nblk;
         if (t_lo > t_hi) t_lo = t_hi;
-        one_row_tiled(qrow, k, v, bi, i, skv, hkv, hi / g, d, causal, off, wl, wr, sc, tile, t_lo, t_hi, mutation, s,
-                      p,
+        one_row_tiled(qrow, k, v, bi, i, skv, hkv, hi / g, d, causal, off, wl, wr, sc, softcap, tile, t_lo, t_hi,
+                      mutation, s, p,
                       o_part + (sp * nrows + r) * d, lse_part + sp * nrows + r);
       }
     }
@@ -336,8 +362,11 @@ int64_t oracle_num_splits(int64_t units, int64_t slots, int64_t nblk, int64_t ma
  * with the same visibility rule as the forward pass; the query heads that share
  * a key/value head add their contributions to its dK / dV.
  *   q, dout: [b][sq][hq][d]; k, v: [b][skv][hkv][d]; outputs dq like q, dk / dv like k.
+ * With softcap c > 0 the scores are capped as in the forward pass and dS gains the
+ * factor 1 - tanh^2(s / c) (the derivative of the cap), read off the capped score.
  * Mutations (test only): 16 drops D, 32 drops the scale from dQ / dK, 64 uses P
- * in place of dS for dK.  Returns 0, or -1 on bad arguments / allocation failure.
+ * in place of dS for dK, 256 drops the softcap factor.  Returns 0, or -1 on bad
+ * arguments / allocation failure.
  */
 #define ORACLE_MUT_BWD_NO_D 16
 #define ORACLE_MUT_BWD_NO_SCALE 32
@@ -345,7 +374,8 @@ int64_t oracle_num_splits(int64_t units, int64_t slots, int64_t nblk, int64_t ma
 
 int oracle_attention_bwd(const double* q, const double* k, const double* v, const double* dout, int64_t b,
                          int64_t sq, int64_t skv, int64_t hq, int64_t hkv, int64_t d, int causal, int64_t off,
-                         int64_t wl, int64_t wr, double scale, double* dq, double* dk, double* dv, int mutation) {
+                         int64_t wl, int64_t wr, double scale, double softcap, double* dq, double* dk, double* dv,
+                         int mutation) {
   if (hkv <= 0 || hq % hkv != 0 || d <= 0 || b < 0 || sq < 0 || skv < 0) return -1;
   const int64_t g = hq / hkv;
   const double gscale = (mutation & ORACLE_MUT_BWD_NO_SCALE) ? 1.0 : scale;
@@ -376,7 +406,7 @@ int oracle_attention_bwd(const double* q, const double* k, const double* v, cons
           int64_t nvis = 0;
           for (int64_t j = 0; j < skv; ++j) {
             if (!oracle_visible_window(i, j, skv, causal, off, wl, wr, 0)) continue;
-            s[j] = scale * dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d);
+            s[j] = capped(dot(qrow, k + ((bi * skv + j) * hkv + kvh) * d, d), scale, softcap, 0);
             if (s[j] > m) m = s[j];
             ++nvis;
           }
@@ -401,7 +431,11 @@ int oracle_attention_bwd(const double* q, const double* k, const double* v, cons
             double* dkrow = dk + ((bi * skv + j) * hkv + kvh) * d;
             double* dvrow = dv + ((bi * skv + j) * hkv + kvh) * d;
             const double dp = dot(dorow, vrow, d);
-            const double ds = p * (dp - D);
+            double ds = p * (dp - D);
+            if (softcap > 0.0 && !(mutation & ORACLE_MUT_CAP_NO_DERIV)) {
+              const double t = s[j] / softcap; /* tanh of the scaled score over c */
+              ds *= 1.0 - t * t;
+            }
             const double dk_coef = (mutation & ORACLE_MUT_BWD_DK_FROM_P) ? p : ds;
             for (int64_t t = 0; t < d; ++t) {
               dvrow[t] += p * dorow[t];
