@@ -91,6 +91,8 @@ typedef struct {
   int32_t local;        /* 0 or 1: apply the sliding window below (ABI version >= 2) */
   int64_t window_left;  /* local: row i sees keys j >= i + q_pos_offset - window_left; -1 = no left edge */
   int64_t window_right; /* local: row i sees keys j <= i + q_pos_offset + window_right; -1 = no right edge */
+  float softcap;        /* 0 = off; c > 0: every scaled score s becomes c * tanh(s / c) before the mask and the
+                           softmax (Is_softcap of "flash attention V2 code walkthrough"; ABI version >= 3) */
 } fa_fwd_args;
 
 /*
@@ -208,6 +210,7 @@ typedef struct {
   float scale;
   int32_t local;                  /* 0 or 1 (ABI version >= 2) */
   int32_t window_left;            /* local: keys at positions >= len_b - 1 - window_left; -1 = all */
+  float softcap;                  /* as in fa_fwd_args (ABI version >= 3) */
 } fa_kvcache_args;
 
 /* Workspace bytes fa_fwd_kvcache needs for num_splits splits (0 = its default); 0 if invalid. */
@@ -257,6 +260,7 @@ typedef struct {
   int64_t window_left;
   int64_t window_right;
   float scale;                    /* finite, > 0 */
+  float softcap;                  /* as in fa_fwd_args (ABI version >= 3) */
 } fa_varlen_args;
 
 /*
@@ -302,6 +306,7 @@ typedef struct {
   float scale;
   int32_t local;
   int64_t window_left, window_right;
+  float softcap;        /* as in fa_fwd_args; dS gains the cap's derivative 1 - tanh^2(s / c) (ABI version >= 3) */
 } fa_bwd_args;
 
 /* Workspace bytes fa_bwd needs (0 for invalid arguments). */

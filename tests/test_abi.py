@@ -39,7 +39,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_version() == 2
+    assert lib.fa_version() == 3
     for code in range(5):
         assert lib.fa_status_string(code)
     assert lib.fa_status_string(99) == b"unknown status"
@@ -74,7 +74,7 @@ def _args(**kw):
 @pytest.mark.parametrize("field,value,expect", [
     ("dtype", 7, 1), ("b", 0, 1), ("hq", 3, 1), ("causal", 2, 1), ("scale", 0.0, 1),
     ("scale", float("nan"), 1), ("d", 96, 2), ("d", 32, 2), ("q", 0, 1), ("lse", 0, 1), ("q", 4100, 1),
-    ("local", 2, 1),
+    ("local", 2, 1), ("softcap", -1.0, 1), ("softcap", float("nan"), 1), ("softcap", float("inf"), 1),
 ])
 def test_validation_rejects_before_any_launch(lib, field, value, expect):
     a = _args(**{field: value})
@@ -192,6 +192,7 @@ def _kv_args(**kw):
 @pytest.mark.parametrize("field,value,expect", [
     ("page_size", 100, 2), ("page_size", -1, 1), ("block_table", 0, 1), ("seqlens_k", 0, 1), ("d", 80, 2),
     ("hq", 7, 1), ("num_pages", 0, 1), ("max_seqlen_k", -5, 1), ("k", 4100, 1), ("scale", 0.0, 1),
+    ("softcap", -2.0, 1), ("softcap", float("nan"), 1),
 ])
 def test_kvcache_validation(lib, field, value, expect):
     a = _kv_args(**{field: value})
@@ -228,6 +229,7 @@ def _varlen_args(**kw):
     ("dtype", 3, 1), ("b", 0, 1), ("hq", 3, 1), ("d", 96, 2), ("total_q", -1, 1), ("max_seqlen_q", -1, 1),
     ("causal", 2, 1), ("local", 2, 1), ("scale", 0.0, 1), ("q", 0, 1), ("cu_seqlens_q", 0, 1),
     ("cu_seqlens_k", 4098, 1), ("k", 4100, 1), ("lse", 0, 1), ("total_k", (1 << 30) + 1, 2),
+    ("softcap", -0.5, 1), ("softcap", float("inf"), 1),
 ])
 def test_varlen_validation(lib, field, value, expect):
     a = _varlen_args(**{field: value})
@@ -265,7 +267,7 @@ def _bwd_args(**kw):
 
 @pytest.mark.parametrize("field,value,expect", [
     ("d", 256, 2), ("d", 96, 2), ("dout", 0, 1), ("dq", 4100, 1), ("dk", 0, 1), ("lse", 0, 1), ("hq", 3, 1),
-    ("causal", 5, 1), ("scale", -1.0, 1),
+    ("causal", 5, 1), ("scale", -1.0, 1), ("softcap", -3.0, 1), ("softcap", float("nan"), 1),
 ])
 def test_bwd_validation(lib, field, value, expect):
     a = _bwd_args(**{field: value})

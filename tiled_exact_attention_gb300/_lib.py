@@ -71,6 +71,7 @@ class FwdArgs(ctypes.Structure):
         ("local", ctypes.c_int32),
         ("window_left", ctypes.c_int64),
         ("window_right", ctypes.c_int64),
+        ("softcap", ctypes.c_float),
     ]
 
 
@@ -102,6 +103,7 @@ class KvcacheArgs(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("local", ctypes.c_int32),
         ("window_left", ctypes.c_int32),
+        ("softcap", ctypes.c_float),
     ]
 
 
@@ -133,6 +135,7 @@ class VarlenArgs(ctypes.Structure):
         ("window_left", ctypes.c_int64),
         ("window_right", ctypes.c_int64),
         ("scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
     ]
 
 
@@ -170,6 +173,7 @@ class BwdArgs(ctypes.Structure):
         ("local", ctypes.c_int32),
         ("window_left", ctypes.c_int64),
         ("window_right", ctypes.c_int64),
+        ("softcap", ctypes.c_float),
     ]
 
 

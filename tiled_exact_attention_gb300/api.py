@@ -47,8 +47,9 @@ def _check_qkv(q, k, v):
 
 
 def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offset: int | None,
-              window=None) -> FwdArgs:
-    """Fill `fa_fwd_args`.  window = (left, right) turns on the sliding window (-1 leaves a side open)."""
+              window=None, softcap: float = 0.0) -> FwdArgs:
+    """Fill `fa_fwd_args`.  window = (left, right) turns on the sliding window (-1 leaves a side open);
+    softcap = c > 0 caps every scaled score s to c * tanh(s / c)."""
     _check_qkv(q, k, v)
     b, sq, hq, d = q.shape
     skv, hkv = k.shape[1], k.shape[2]
@@ -64,6 +65,7 @@ def make_args(q, k, v, o, lse, *, causal: bool, scale: float | None, q_pos_offse
     if window is not None:
         a.local = 1
         a.window_left, a.window_right = int(window[0]), int(window[1])
+    a.softcap = float(softcap)
     return a
 
 
@@ -81,10 +83,11 @@ def _outputs(q, out, lse):
 
 
 def fa_fwd(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
-           out=None, lse=None, stream=None, window=None):
+           out=None, lse=None, stream=None, window=None, softcap: float = 0.0):
     """Forward pass; returns (O, LSE)."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window,
+                  softcap=softcap)
     check(_lib.load().fa_fwd(ctypes.byref(a), _stream_handle(stream)), "fa_fwd")
     return out, lse
 
@@ -93,25 +96,29 @@ def fa_num_splits_heuristic(units: int, slots: int, num_kv_blocks: int, max_spli
     return int(_lib.load().fa_num_splits_heuristic(units, slots, num_kv_blocks, max_splits))
 
 
-def fa_splitkv_default_splits(q, k, v, *, causal=False, scale=None, q_pos_offset=None, window=None) -> int:
+def fa_splitkv_default_splits(q, k, v, *, causal=False, scale=None, q_pos_offset=None, window=None,
+                              softcap: float = 0.0) -> int:
     out, lse = _outputs(q, None, None)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window,
+                  softcap=softcap)
     return int(_lib.load().fa_splitkv_default_splits(ctypes.byref(a)))
 
 
 def fa_splitkv_workspace_size(q, k, v, num_splits: int = 0, *, causal=False, scale=None,
-                              q_pos_offset=None, window=None) -> int:
+                              q_pos_offset=None, window=None, softcap: float = 0.0) -> int:
     out, lse = _outputs(q, None, None)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window,
+                  softcap=softcap)
     return int(_lib.load().fa_splitkv_workspace_size(ctypes.byref(a), num_splits))
 
 
 def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None, q_pos_offset: int | None = None,
                    num_splits: int = 0, workspace=None, out=None, lse=None, stream=None, return_splits=False,
-                   window=None):
+                   window=None, softcap: float = 0.0):
     """Split-KV forward + combine; returns (O, LSE) (and the split count if asked)."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window,
+                  softcap=softcap)
     lib = _lib.load()
     need = int(lib.fa_splitkv_workspace_size(ctypes.byref(a), int(num_splits)))
     if workspace is None:
@@ -127,10 +134,11 @@ def fa_fwd_splitkv(q, k, v, *, causal: bool = False, scale: float | None = None,
 
 def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None = None,
                            q_pos_offset: int | None = None, num_splits: int = 0, out=None, lse=None, stream=None,
-                           return_splits=False, window=None):
+                           return_splits=False, window=None, softcap: float = 0.0):
     """Split-KV forward that uses the library's built-in scratch instead of a workspace."""
     out, lse = _outputs(q, out, lse)
-    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window)
+    a = make_args(q, k, v, out, lse, causal=causal, scale=scale, q_pos_offset=q_pos_offset, window=window,
+                  softcap=softcap)
     used = ctypes.c_int32(0)
     check(_lib.load().fa_fwd_splitkv_noalloc(ctypes.byref(a), int(num_splits), ctypes.byref(used),
                                              _stream_handle(stream)), "fa_fwd_splitkv_noalloc")
@@ -140,7 +148,8 @@ def fa_fwd_splitkv_noalloc(q, k, v, *, causal: bool = False, scale: float | None
 
 
 def make_kvcache_args(q, k, v, o, lse, *, block_table=None, seqlens_k=None, cu_seqlens_k=None,
-                      max_seqlen_k: int = 0, scale: float | None = None, window_left=None) -> KvcacheArgs:
+                      max_seqlen_k: int = 0, scale: float | None = None, window_left=None,
+                      softcap: float = 0.0) -> KvcacheArgs:
     """Fill `fa_kvcache_args`.  q, o: [b, hq, d]; paged k/v: [num_pages, page_size, hkv, d] with
     block_table [b, n] and seqlens_k [b] (int32); packed k/v: [total_k, hkv, d] with cu_seqlens_k [b + 1].
     window_left (not None) keeps only the last window_left + 1 keys of each sequence."""
@@ -184,12 +193,13 @@ def make_kvcache_args(q, k, v, o, lse, *, block_table=None, seqlens_k=None, cu_s
     a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     if window_left is not None:
         a.local, a.window_left = 1, int(window_left)
+    a.softcap = float(softcap)
     return a
 
 
 def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=None, max_seqlen_k=None,
                    scale=None, num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
-                   return_splits=False, window_left=None):
+                   return_splits=False, window_left=None, softcap: float = 0.0):
     """Decode one query row per sequence against a paged or packed KV cache; returns (O [b, hq, d], LSE [b, hq])."""
     if out is None:
         out = torch.empty_like(q)
@@ -200,7 +210,7 @@ def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=No
         max_seqlen_k = int(lens.max().item()) if lens.numel() else 0
     a = make_kvcache_args(q, k, v, out, lse, block_table=block_table, seqlens_k=seqlens_k,
                           cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, scale=scale,
-                          window_left=window_left)
+                          window_left=window_left, softcap=softcap)
     lib = _lib.load()
     if workspace is None:
         need = int(lib.fa_kvcache_workspace_size(ctypes.byref(a), int(num_splits)))
@@ -215,7 +225,7 @@ def fa_fwd_kvcache(q, k, v, *, block_table=None, seqlens_k=None, cu_seqlens_k=No
 
 
 def make_varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, causal: bool,
-                     scale: float | None, window=None) -> VarlenArgs:
+                     scale: float | None, window=None, softcap: float = 0.0) -> VarlenArgs:
     """Fill `fa_varlen_args`.  q, o: [total_q, hq, d]; k, v: [total_k, hkv, d]; lse: fp32 [hq, total_q];
     cu_seqlens_q / cu_seqlens_k: CUDA int32 [b + 1] prefix sums."""
     for name, t in (("q", q), ("k", k), ("v", v), ("out", o)):
@@ -251,11 +261,12 @@ def make_varlen_args(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_
         a.local = 1
         a.window_left, a.window_right = int(window[0]), int(window[1])
     a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    a.softcap = float(softcap)
     return a
 
 
 def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int | None = None, causal: bool = False,
-                  scale: float | None = None, window=None, out=None, lse=None, stream=None):
+                  scale: float | None = None, window=None, out=None, lse=None, stream=None, softcap: float = 0.0):
     """Forward pass over packed variable-length sequences; returns (O [total_q, hq, d], LSE [hq, total_q]).
     max_seqlen_q defaults to the longest sequence (read back from the device once)."""
     if out is None:
@@ -266,13 +277,13 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int | No
         lens = cu_seqlens_q[1:] - cu_seqlens_q[:-1]
         max_seqlen_q = int(lens.max().item()) if lens.numel() else 0
     a = make_varlen_args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=max_seqlen_q, causal=causal,
-                         scale=scale, window=window)
+                         scale=scale, window=window, softcap=softcap)
     check(_lib.load().fa_fwd_varlen(ctypes.byref(a), _stream_handle(stream)), "fa_fwd_varlen")
     return out, lse
 
 
 def make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, *, causal: bool, scale: float | None,
-                  q_pos_offset: int | None, window=None) -> BwdArgs:
+                  q_pos_offset: int | None, window=None, softcap: float = 0.0) -> BwdArgs:
     """Fill `fa_bwd_args` from [b, s, h, d] tensors (lse fp32 [b, hq, sq])."""
     _check_qkv(q, k, v)
     for name, t, like in (("o", o, q), ("dout", dout, q), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
@@ -296,17 +307,19 @@ def make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, *, causal: bool, scale: flo
     if window is not None:
         a.local = 1
         a.window_left, a.window_right = int(window[0]), int(window[1])
+    a.softcap = float(softcap)
     return a
 
 
 def fa_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
-           q_pos_offset: int | None = None, window=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+           q_pos_offset: int | None = None, window=None, dq=None, dk=None, dv=None, workspace=None, stream=None,
+           softcap: float = 0.0):
     """Backward pass for the forward call with the same arguments; returns (dQ, dK, dV)."""
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     a = make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, scale=scale, q_pos_offset=q_pos_offset,
-                      window=window)
+                      window=window, softcap=softcap)
     lib = _lib.load()
     if workspace is None:
         need = int(lib.fa_bwd_workspace_size(ctypes.byref(a)))

@@ -81,6 +81,23 @@ bool strides_ok(const int64_t s[3]) {
   return true;
 }
 
+// softcap: 0 (off) or a finite positive cap
+bool softcap_ok(float c) { return c == 0.f || (c > 0.f && std::isfinite(c)); }
+
+// Softcap constants for a kernel whose score x relates to the scaled score s by
+// s = s_per_x * x: tanh(s / c) = 1 - 2 / (2^(k x) + 1) with k = 2 log2(e) s_per_x / c,
+// and the capped score in log2 units is b tanh(s / c) with b = c log2(e).  c = 0: off.
+void softcap_consts(float c, double s_per_x, float* k, float* b) {
+  constexpr double kLog2eD = 1.4426950408889634;
+  if (!(c > 0.f)) {
+    *k = 0.f;
+    *b = 0.f;
+    return;
+  }
+  *k = static_cast<float>(2.0 * kLog2eD * s_per_x / static_cast<double>(c));
+  *b = static_cast<float>(static_cast<double>(c) * kLog2eD);
+}
+
 fa_status validate(const fa_fwd_args* a) {
   if (a == nullptr) return FA_ERR_INVALID_ARG;
   if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
@@ -90,6 +107,7 @@ fa_status validate(const fa_fwd_args* a) {
   if (a->local != 0 && a->local != 1) return FA_ERR_INVALID_ARG;
   if (a->local && (a->window_left < -1 || a->window_right < -1)) return FA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (!softcap_ok(a->softcap)) return FA_ERR_INVALID_ARG;
   if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->sq > (1 << 30) || a->skv > (1 << 30)) return FA_ERR_UNSUPPORTED;
   if (a->sq == 0) return FA_OK;
@@ -263,6 +281,7 @@ fa_status validate_kvcache(const fa_kvcache_args* a) {
   if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
   if (a->b < 1 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (!softcap_ok(a->softcap)) return FA_ERR_INVALID_ARG;
   if ((a->local != 0 && a->local != 1) || (a->local && a->window_left < -1)) return FA_ERR_INVALID_ARG;
   if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->max_seqlen_k < 0 || a->max_seqlen_k > (1 << 30) || a->num_pages < 1) return FA_ERR_INVALID_ARG;
@@ -304,6 +323,7 @@ fa_status validate_varlen(const fa_varlen_args* a) {
   if (a->local != 0 && a->local != 1) return FA_ERR_INVALID_ARG;
   if (a->local && (a->window_left < -1 || a->window_right < -1)) return FA_ERR_INVALID_ARG;
   if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (!softcap_ok(a->softcap)) return FA_ERR_INVALID_ARG;
   if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->total_q > (1 << 30) || a->total_k > (1 << 30) || a->max_seqlen_q > (1 << 30)) return FA_ERR_UNSUPPORTED;
   if (a->total_q == 0 || a->max_seqlen_q == 0) return FA_OK;
@@ -352,7 +372,7 @@ using namespace fa;
 
 extern "C" {
 
-int32_t fa_version(void) { return 2; }
+int32_t fa_version(void) { return 3; }
 
 const char* fa_status_string(fa_status s) {
   switch (s) {
@@ -416,6 +436,7 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   p.local = c.local;
   p.left_off = c.left_off;
   p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
   p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
   p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
   p.num_splits = 1;
@@ -517,6 +538,7 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     const int span = p.nblk - p.kv_start / bn;
     p.blocks_per_split = static_cast<int>(ceil_div64(span > 0 ? span : 1, ns));
     p.scale_log2 = scale_log2;
+    softcap_consts(a->softcap, 1.0 / 1.4426950408889634, &p.sc_k, &p.sc_b);  // (scores arrive times scale log2 e)
     p.status = di.status;
     p.box_rows = bn;
     p.counters = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(lse_part) + align256(rows * sizeof(float)));
@@ -554,6 +576,7 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     p.local = c.local;
     p.left_off = c.left_off;
     p.scale_log2 = scale_log2;
+    softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
     p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
     p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
     p.num_splits = ns;
@@ -632,6 +655,7 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
   p.num_splits = ns;
   p.blocks_per_split = 1;  // set per sequence in the kernel
   p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  softcap_consts(a->softcap, 1.0 / 1.4426950408889634, &p.sc_k, &p.sc_b);  // (scores arrive times scale log2 e)
   p.status = di.status;
   p.kv_mode = paged ? kKvPaged : kKvPacked;
   p.block_table = a->block_table;
@@ -710,6 +734,7 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   p.hkv = a->hkv;
   p.g = a->hq / a->hkv;
   p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
   p.n_mtiles = static_cast<int>(ceil_div64(a->max_seqlen_q, 128));
   p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
   p.num_splits = 1;
@@ -753,6 +778,7 @@ fa_fwd_args fwd_view(const fa_bwd_args* a) {
   f.local = a->local;
   f.window_left = a->window_left;
   f.window_right = a->window_right;
+  f.softcap = a->softcap;
   return f;
 }
 
@@ -840,6 +866,7 @@ fa_status fa_bwd(const fa_bwd_args* a, void* workspace, size_t workspace_bytes, 
   p.left_off = c.left_off;
   p.scale = a->scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
   const size_t rows = static_cast<size_t>(a->b) * a->hq * p.sq_pad;
   p.dpre = static_cast<float*>(workspace);
   p.l2pre = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * sizeof(float)));

@@ -196,7 +196,8 @@ __device__ __forceinline__ void key_block_range(const BwdParams& p, int row0, in
   *hi = h;
 }
 
-template <int D, bool BF16>
+// SC: softcap; the score is capped to c tanh(s / c) and dS gains the factor 1 - tanh^2.
+template <int D, bool BF16, bool SC>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM, BN = C::BN, ST = C::DQ_STAGES;
@@ -386,14 +387,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           // pairs of keys in packed f32x2 math; the mask only where an edge cuts the chunk
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv2[hf][i]), __uint_as_float(sv2[hf][i + 1])),
-                                      make_float2(sl2, sl2), make_float2(-l2, -l2));
+          float2 x, w = make_float2(1.f, 1.f);
+          if constexpr (SC) {
+            // capped score c log2(e) tanh(s / c); dS gains w = 1 - tanh^2
+            const float t0 = tanh_from_exp2_arg(__uint_as_float(sv2[hf][i]) * p.sc_k);
+            const float t1 = tanh_from_exp2_arg(__uint_as_float(sv2[hf][i + 1]) * p.sc_k);
+            x = make_float2(fmaf(p.sc_b, t0, -l2), fmaf(p.sc_b, t1, -l2));
+            w = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+          } else {
+            x = __ffma2_rn(make_float2(__uint_as_float(sv2[hf][i]), __uint_as_float(sv2[hf][i + 1])),
+                           make_float2(sl2, sl2), make_float2(-l2, -l2));
+          }
           float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (edge) {
             const int c = c0 + i;
             if (c >= lim || c < lo) pr.x = 0.f;
             if (c + 1 >= lim || c + 1 < lo) pr.y = 0.f;
           }
+          if constexpr (SC) pr = __fmul2_rn(pr, w);
           pf[hf][i] = pr.x;
           pf[hf][i + 1] = pr.y;
         }
@@ -462,7 +473,7 @@ __device__ __forceinline__ void query_tile_range(const BwdParams& p, int j0, int
   *hi = h;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SC>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM, BN = C::BN, ST = C::KV_STAGES;
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
       tmem_ld_wait();
       reg_fence<32>(sv[0]);
       reg_fence<32>(sv[1]);
-      float pf[2][32];  // P in fp32, kept for dS
+      float pf[2][32];  // P in fp32 (times 1 - tanh^2 under softcap), kept for dS
       const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -680,17 +691,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const float2 nl = e == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[hf][i + e]), __uint_as_float(sv[hf][i + e + 1])),
-                                        sl2v, nl);
+            float2 x, w = make_float2(1.f, 1.f);
+            if constexpr (SC) {
+              // capped score c log2(e) tanh(s / c); dS gains w = 1 - tanh^2
+              const float t0 = tanh_from_exp2_arg(__uint_as_float(sv[hf][i + e]) * p.sc_k);
+              const float t1 = tanh_from_exp2_arg(__uint_as_float(sv[hf][i + e + 1]) * p.sc_k);
+              x = make_float2(fmaf(p.sc_b, t0, nl.x), fmaf(p.sc_b, t1, nl.y));
+              w = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+            } else {
+              x = __ffma2_rn(make_float2(__uint_as_float(sv[hf][i + e]), __uint_as_float(sv[hf][i + e + 1])), sl2v,
+                             nl);
+            }
             float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if (edge) {
               const int c = c0 + i + e;
               if (c < cmin || c > cmax) pr.x = 0.f;
               if (c + 1 < cmin || c + 1 > cmax) pr.y = 0.f;
             }
+            pp[(i + e) / 2] = pack2<BF16>(pr.x, pr.y);
+            if constexpr (SC) pr = __fmul2_rn(pr, w);  // (P itself goes to dV; P w to dS)
             pf[hf][i + e] = pr.x;
             pf[hf][i + e + 1] = pr.y;
-            pp[(i + e) / 2] = pack2<BF16>(pr.x, pr.y);
           }
         }
         tmem_st16(tS + c0, pp);
@@ -771,7 +792,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_dq_kernel<D, BF16>;
+    auto kern = p.sc_b > 0.f ? fa_bwd_dq_kernel<D, BF16, true> : fa_bwd_dq_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DQ_SMEM);
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(p.n_mtiles) * p.b * p.hq;
@@ -781,7 +802,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
-    auto kern = fa_bwd_dkdv_kernel<D, BF16>;
+    auto kern = p.sc_b > 0.f ? fa_bwd_dkdv_kernel<D, BF16, true> : fa_bwd_dkdv_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(p.n_ntiles) * p.b * p.hkv;

@@ -90,7 +90,7 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t idx) {
 
 enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
 
-template <int D, int G, bool BF16>
+template <int D, int G, bool BF16, bool SC>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit);
@@ -103,7 +103,8 @@ constexpr int dec_smem_bytes() {
          128;
 }
 
-template <int D, int G, bool BF16>
+// SC: softcap, each score capped to c tanh(s / c) before the mask.
+template <int D, int G, bool BF16, bool SC>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecCfg<D>;
   using L = DecLane<D, G>;
@@ -221,8 +222,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
     // ------------------------------ compute warps ------------------------------
     // (each register budget covers only its own role's code)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_COMPUTE));
-    compute_split<D, G, BF16>(p, smem, full, empty, red, flags, warp, lane, split, bi, kvh, h_first, blk_lo, nb,
-                              start, limit);
+    compute_split<D, G, BF16, SC>(p, smem, full, empty, red, flags, warp, lane, split, bi, kvh, h_first, blk_lo, nb,
+                                  start, limit);
   }
 }
 
@@ -278,7 +279,7 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, float* wts, 
   }
 }
 
-template <int D, int G, bool BF16>
+template <int D, int G, bool BF16, bool SC>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit) {
@@ -359,6 +360,11 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
       for (int x = 1; x < L::LPR; x <<= 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] += __shfl_xor_sync(0xffffffffu, sc[ps][h], x);
+      if constexpr (SC) {
+        // capped scores (log2 units): c log2(e) tanh(s / c), before the mask
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[ps][h] = p.sc_b * tanh_from_exp2_arg(sc[ps][h] * p.sc_k);
+      }
       const int key = key0 + ps * L::RPP + rg;
       if (key >= limit || key < start) {
 #pragma unroll
@@ -489,7 +495,7 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
 template <int D, int G, bool BF16>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
-  auto kern = fa_decode_kernel<D, G, BF16>;
+  auto kern = p.sc_b > 0.f ? fa_decode_kernel<D, G, BF16, true> : fa_decode_kernel<D, G, BF16, false>;
   const int smem = dec_smem_bytes<D, G>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -502,7 +508,7 @@ template <int D, int G, bool BF16>
 int dec_occupancy() {
   using C = DecCfg<D>;
   const int smem = dec_smem_bytes<D, G>();
-  auto kern = fa_decode_kernel<D, G, BF16>;
+  auto kern = fa_decode_kernel<D, G, BF16, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem) != cudaSuccess || n < 1) return 1;

@@ -43,6 +43,9 @@ struct PrefillParams {
   const float* k_descale;  // [b][hkv][n_kblocks]
   const float* v_descale;  // [b][hkv]
   int n_kblocks;
+  // Softcap (sc_b > 0): the raw score x = q.k becomes, in log2 units,
+  // sc_b * tanh(s / c) with tanh(s / c) = 1 - 2 / (2^(sc_k x) + 1); sc_b = c log2(e).
+  float sc_k, sc_b;
 };
 
 // Where the decode kernel finds a sequence's keys.
@@ -83,6 +86,9 @@ struct DecodeParams {
   void* o;                      // [b][1][hq][d] of the input type
   int64_t o_stride_b, o_stride_h;
   float* lse;                   // [b][hq], or null
+  // Softcap (sc_b > 0): the score x (q.k * scale * log2 e) becomes sc_b * tanh(x / sc_b),
+  // tanh through 2^(sc_k x) with sc_k = 2 / c; sc_b = c log2(e).
+  float sc_k, sc_b;
 };
 
 // Parameters of the backward kernels (recompute form: D and log2-scaled LSE per
@@ -108,6 +114,7 @@ struct BwdParams {
   float scale, scale_log2;
   int n_mtiles, n_ntiles;  // 128-row query tiles, 128-key blocks
   int* status;
+  float sc_k, sc_b;     // softcap as in PrefillParams (sc_b = 0: off)
 };
 
 // e4m3 quantisation of one [b][s][h][d] tensor.

@@ -205,7 +205,9 @@ __device__ __forceinline__ int item_of(int j) {
 // item's Q as soon as the last S MMA of the current item has read Q, and the MMA
 // warp starts the next item's S MMAs while the softmax warps write the current
 // item's output (its PV MMAs wait only until the previous O has been read out).
-template <int D, bool BF16, bool VARLEN, bool E8 = false>
+// SC: softcap, each score capped to c tanh(s / c) before the mask (a separate
+// instantiation: two more special-function operations per score).
+template <int D, bool BF16, bool VARLEN, bool E8 = false, bool SC = false>
 __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D, E8>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
@@ -519,6 +521,11 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         uint32_t sr[BN];
         tmem_load_row<BN>(tS, sr);
         float* s = reinterpret_cast<float*>(sr);
+        if constexpr (SC) {
+          // capped scores in log2 units, c log2(e) tanh(s / c), before the mask sets -inf
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = p.sc_b * tanh_from_exp2_arg(s[c] * p.sc_k);
+        }
         const bool masked = (n + 1) * BN > skv || (p.causal && (n + 1) * BN - 1 > row0 + off);
         if (masked) {
           const int lim = lim_row - n * BN;
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         // The reference max moves only when the block max exceeds it by more than
         // 2^kRescaleLog2 (exact: l and o share the reference, so O = o / l is
         // unchanged); probabilities stay below 2^kRescaleLog2.
-        const float bm2 = bmax * sl2b;
+        const float bm2 = SC ? bmax : bmax * sl2b;  // (capped scores are already scaled, in log2 units)
         const bool grow = bm2 > m_run + kRescaleLog2;
         const float m_new = grow ? bm2 : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         // P = 2^(s * scale * log2 e - m), written over the first half of the S
         // columns as packed 16-bit pairs; the MMA warp is signalled once per block
         // (a second, earlier signal for half of P measured slower).
-        const float2 sl2v = make_float2(sl2b, sl2b);
+        const float2 sl2v = SC ? make_float2(1.f, 1.f) : make_float2(sl2b, sl2b);
         const float2 negm = make_float2(-m_use, -m_use);
         float2 sum2[4];
 #pragma unroll
@@ -735,7 +742,9 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>;
+  auto kern = p.sc_b > 0.f ? (p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true, false, true>
+                                                : fa_prefill_kernel<D, BF16, false, false, true>)
+                           : (p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;

@@ -371,4 +371,17 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(z) from the identity tanh(z) = 1 - 2 / (e^(2z) + 1), given u = 2 z log2(e):
+// exact at both saturations (u -> +inf gives 1, u -> -inf gives -1), absolute error
+// ~1e-7 elsewhere (the cap multiplies it by c, far below the 16-bit rounding of P).
+__device__ __forceinline__ float tanh_from_exp2_arg(float u) {
+  return fmaf(-2.f, rcp_approx(ex2_approx(u) + 1.f), 1.f);
+}
+
 }  // namespace fa
