@@ -244,6 +244,8 @@ def run_ours(args):
     paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
     bwd = bench_backward(dev, flush, steps=max(10, min(100, K // 50)))
     e4m3 = bench_e4m3(dev, flush, steps=max(10, min(200, K // 25)))
+    variants = bench_variants(dev, flush, float(_peaks()[0].get("bf16_tflops_sustained", _peaks()[0]["bf16_tflops"])),
+                              steps=max(10, min(100, K // 50)))
 
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
     kv_bytes = 2 * wd.b * wd.hkv * wd.skv * wd.d * 2
@@ -314,6 +316,7 @@ def run_ours(args):
                                         "frac_of_burst": round(bwd["value"] / pk_burst, 4),
                                         "traffic": _profiled_traffic("fa_bwd_dkdv_kernel"),
                                         "traffic_kernel": "fa_bwd_dkdv_kernel (the larger of the two product kernels)"}),
+        "variants": variants,
         "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
                      "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
                      "kernel": "fa_prefill_kernel<128, bf16>",
@@ -414,6 +417,83 @@ def bench_e4m3(dev, flush, steps=30, warmup=3):
             "dtype": "e4m3 inputs, e4m3 P, fp32 accumulation, bf16 O",
             "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "causal": True},
             "flops_per_launch": flops, "kernel": "fa_prefill_kernel<128, bf16, dense, e4m3>", "steps": steps}
+
+
+def _timed(step, flush, steps, warmup=3):
+    """Mean CUDA-event time (ms) of `step` over `steps` calls, L2 flushed before each."""
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+
+
+def bench_variants(dev, flush, pk, steps=20):
+    """The mask and layout variants of the forward pass, each on a prefill-sized problem, in TFLOP/s of the
+    visible (query, key) pairs (4 d flops per pair and head), against the sustained bf16 peak:
+      * window: the causal prefill workload with a sliding window of 1024 keys (local causal);
+      * softcap: the causal prefill workload with every score capped to 30 tanh(s / 30);
+      * varlen: 16 packed causal sequences, lengths drawn (seeded) from [256, 4096], H = 16, d = 128."""
+    import numpy as np
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_fwd, fa_fwd_varlen, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import BASE_SEED, WORKLOADS, make_qkv, normal
+
+    w = WORKLOADS["causal_prefill"]
+    q, k, v = (t.to(dev) for t in make_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.b, w.hq, w.sq), dtype=torch.float32, device=dev)
+    out = {}
+    wl = 1024
+    i = np.arange(w.sq, dtype=np.int64)
+    pairs = int((np.minimum(i, wl) + 1).sum())  # row i sees keys max(0, i - wl) .. i
+    ms = _timed(lambda: fa_fwd(q, k, v, causal=True, window=(wl, 0), out=o, lse=lse), flush, steps)
+    tf = 4.0 * w.d * pairs * w.b * w.hq / (ms * 1e-3) / 1e12
+    out["window"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+                     "config": {"b": w.b, "sq": w.sq, "hq": w.hq, "d": w.d, "causal": True, "window": [wl, 0]},
+                     "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
+                                  "frac": round(tf / pk, 4), "traffic": None}}
+    pairs = w.visible_pairs_per_head()
+    ms = _timed(lambda: fa_fwd(q, k, v, causal=True, softcap=30.0, out=o, lse=lse), flush, steps)
+    tf = 4.0 * w.d * pairs * w.b * w.hq / (ms * 1e-3) / 1e12
+    out["softcap"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+                      "config": {"b": w.b, "sq": w.sq, "hq": w.hq, "d": w.d, "causal": True, "softcap": 30.0},
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
+                                   "frac": round(tf / pk, 4), "traffic": None}}
+    rng = np.random.default_rng(BASE_SEED + 60)
+    lens = rng.integers(256, 4097, size=16).astype(np.int64)
+    total = int(lens.sum())
+    hq, d = 16, 128
+    qv = normal((total, hq, d), BASE_SEED + 60, 0).to(dev)
+    kv = normal((total, hq, d), BASE_SEED + 60, 1).to(dev)
+    vv = normal((total, hq, d), BASE_SEED + 60, 2).to(dev)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(dev)
+    ov = torch.empty_like(qv)
+    lv = torch.empty((hq, total), dtype=torch.float32, device=dev)
+    mx = int(lens.max())
+    ms = _timed(lambda: fa_fwd_varlen(qv, kv, vv, cu, cu, max_seqlen_q=mx, causal=True, out=ov, lse=lv), flush,
+                steps)
+    pairs = int((lens * (lens + 1) // 2).sum())
+    tf = 4.0 * d * pairs * hq / (ms * 1e-3) / 1e12
+    out["varlen"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+                     "config": {"sequences": len(lens), "lengths": [int(x) for x in lens], "hq": hq, "d": d,
+                                "causal": True},
+                     "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
+                                  "frac": round(tf / pk, 4), "traffic": None}}
+    if fa_sync_status() != 0:
+        raise RuntimeError("device status set by a forward-pass variant")
+    return out
 
 
 def bench_e2e(qc, kc, vc, wp, fa_fwd, flush, stream, steps, dist=None):
