@@ -601,13 +601,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
                                                         true);
         issue_pv_tile<D, BM, C::TILE_BYTES, kIdA, 6, 8>(tbase + C::ACC_COL, tbase + C::S_COL + 48, domn_desc, 0,
                                                         true);
-        // the next tile's S^T = K Q^T over the columns dV has just read
-        if (more) {
-          if (!mbar_wait(&qd_full[s1], ((ti + 1) / ST) & 1, p.status, kSiteBwdQdFull)) break;
+        // the next tile's S^T = K Q^T over the columns dV has just read: here if its
+        // Q / dO stage has landed, else after dK (anywhere after dV keeps the order)
+        bool s_issued = false;
+        if (more && mbar_test(&qd_full[s1], ((ti + 1) / ST) & 1)) {
           tc_fence_after();
           issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(
               tbase + C::S_COL, FA_KDESC(), sdesc_sw128(opaque_u32(smem_u32(stage_ptr(s1))), 16, 1024), 0, 0);
           umma_commit(s_full);
+          s_issued = true;
         }
         // dK += dS^T Q, likewise by halves; Q read MN-major
         if (!mbar_wait(&ds_half[0], ti & 1, p.status, kSiteBwdDsFull)) break;
@@ -624,6 +626,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
                                                         true);
         // the next tile's dP^T = V dO^T over the columns dK has just read
         if (more) {
+          if (!s_issued) {
+            if (!mbar_wait(&qd_full[s1], ((ti + 1) / ST) & 1, p.status, kSiteBwdQdFull)) break;
+            tc_fence_after();
+            issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(
+                tbase + C::S_COL, FA_KDESC(), sdesc_sw128(opaque_u32(smem_u32(stage_ptr(s1))), 16, 1024), 0, 0);
+            umma_commit(s_full);
+          }
           issue_s_tile<D, BM, BN, C::TILE_BYTES, C::TILE_BYTES, kIdS>(
               tbase + C::DP_COL, FA_VDESC(), sdesc_sw128(opaque_u32(smem_u32(stage_ptr(s1))) + C::TILE_BYTES, 16, 1024),
               0, 0);
