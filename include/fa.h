@@ -146,7 +146,9 @@ size_t fa_splitkv_workspace_size(const fa_fwd_args* args, int32_t num_splits);
  * sharing a KV head are folded into one CTA (section 7.4).  num_splits == 0 picks the count with the heuristic;
  * the count used is written to *splits_used (may be NULL).  The workspace is a
  * caller-owned device buffer of at least fa_splitkv_workspace_size bytes,
- * 256-byte aligned.  Same result as fa_fwd up to rounding.
+ * 256-byte aligned, needing no initialisation; two calls whose work overlaps on
+ * the GPU (different streams) need different workspaces.  Same result as fa_fwd
+ * up to rounding.
  */
 fa_status fa_fwd_splitkv(const fa_fwd_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
                          int32_t* splits_used, void* stream);
@@ -223,7 +225,7 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits
  * and cut into num_splits ranges of that sequence's own length (0 = the
  * split-count heuristic, applied with max_seqlen_k), merged inside the split
  * kernel as for fa_fwd_splitkv with sq == 1.  The workspace is caller-owned device memory of at least
- * fa_kvcache_workspace_size bytes, 256-byte aligned.
+ * fa_kvcache_workspace_size bytes, 256-byte aligned, under the same rules as fa_fwd_splitkv's.
  */
 fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
                          int32_t* splits_used, void* stream);
