@@ -178,6 +178,8 @@ SPLIT_CASES = [
     (3, 1, 129, 3, 1, 128, "bf16", False, None, 2),
     (1, 1, 200, 4, 4, 128, "bf16", True, -5, 3),
     (1, 40, 600, 4, 2, 128, "bf16", True, None, 3),
+    (1, 40, 600, 4, 2, 128, "bf16", True, None, 1),
+    (2, 1, 900, 16, 2, 128, "bf16", True, 600, 1),
     (2, 130, 300, 2, 2, 64, "fp16", False, None, 2),
     (1, 200, 256, 2, 1, 256, "bf16", True, None, 4),
 ]

@@ -201,7 +201,21 @@ MaskPlan plan_mask(const fa_fwd_args* a) {
   return c;
 }
 
-bool use_decode_kernel(const fa_fwd_args* a) { return a->sq == 1 && decode_supported(a->d, a->hq / a->hkv); }
+// One query row (sq == 1) with many query heads per KV head and no sliding
+// window: Q is viewed as g rows of hkv heads, so the g query heads sharing a KV
+// head become the rows of one tensor-core tile of the prefill kernel ("ai-reference-
+// codex: forward CUDA kernel", 7.4; "flash attention V2 code walkthrough", the
+// ngroups > 1 launch).  Smaller groups stay on the CUDA-core decode kernel: a
+// 128-row tile would be mostly padding, while that kernel's arithmetic per KV
+// byte grows only with g.
+constexpr int kHeadRowsMinG = 8;
+bool use_head_rows(const fa_fwd_args* a) {
+  return a->sq == 1 && a->hq / a->hkv >= kHeadRowsMinG && !plan_mask(a).local;
+}
+
+bool use_decode_kernel(const fa_fwd_args* a) {
+  return a->sq == 1 && !use_head_rows(a) && decode_supported(a->d, a->hq / a->hkv);
+}
 
 // Keys a decode row can see (sq == 1): kv_start <= j < kv_limit.
 int decode_kv_limit(const fa_fwd_args* a) {
@@ -225,7 +239,13 @@ struct SplitShape {
 };
 
 bool split_shape(const fa_fwd_args* a, const DeviceInfo& di, SplitShape* s) {
-  if (use_decode_kernel(a)) {
+  if (use_head_rows(a)) {
+    const int g = a->hq / a->hkv;
+    const int64_t n_mcta = ceil_div64(ceil_div64(g, 128), prefill_q_tiles(a->d));
+    s->units = static_cast<int64_t>(a->b) * a->hkv * n_mcta;
+    s->slots = di.sms;
+    s->nblk = ceil_div64(decode_kv_limit(a), prefill_block_n(a->d));
+  } else if (use_decode_kernel(a)) {
     const int g = a->hq / a->hkv;
     s->units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
     s->slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
@@ -512,7 +532,55 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
   cudaError_t e;
-  if (use_decode_kernel(a)) {
+  if (use_head_rows(a)) {
+    // Q viewed as [b][g rows][hkv heads][d]: row r of head kvh is query head kvh * g + r,
+    // and every row sees the same keys j < kv_limit (no per-row mask)
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int g = a->hq / a->hkv;
+    const int bn = prefill_block_n(a->d);
+    const int64_t q_view[3] = {a->q_strides[0], a->q_strides[2], static_cast<int64_t>(g) * a->q_strides[2]};
+    if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hkv, g, a->b, q_view, 64, 128, true)) return FA_ERR_INVALID_ARG;
+    if (a->skv > 0 &&
+        (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, a->skv, a->b, a->k_strides, 64, bn, true) ||
+         !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, a->skv, a->b, a->v_strides, 64, bn, true)))
+      return FA_ERR_INVALID_ARG;
+    const int lim = decode_kv_limit(a);
+    if (ns == 1) {
+      // one split: the kernel writes O and LSE itself, through the same view of O
+      // (LSE [b][hkv][g] is [b][hq][1])
+      p.o = a->o;
+      p.lse = a->lse;
+      p.o_stride_b = a->o_strides[0];
+      p.o_stride_row = a->o_strides[2];
+      p.o_stride_h = static_cast<int64_t>(g) * a->o_strides[2];
+      p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[2] % 16 == 0;
+    } else {
+      p.lse = lse_part;  // partials [ns][b][hkv][g] = [ns][b][hq]: the layout the combine reads
+      p.o_part = o_part;
+    }
+    p.b = a->b;
+    p.sq = g;
+    p.skv = lim;
+    p.hq = a->hkv;
+    p.hkv = a->hkv;
+    p.g = 1;
+    p.scale_log2 = scale_log2;
+    softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
+    p.n_mtiles = static_cast<int>(ceil_div64(g, 128));
+    p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+    p.num_splits = ns;
+    const int64_t nblk = ceil_div64(lim, bn);
+    p.blocks_per_split = static_cast<int>(ceil_div64(nblk > 0 ? nblk : 1, ns));
+    p.max_ctas = di.sms;
+    p.status = di.status;
+    e = launch_prefill(p, a->d, a->dtype, st);
+    if (ns == 1) {
+      if (e != cudaSuccess) return FA_ERR_CUDA;
+      if (splits_used) *splits_used = 1;
+      return FA_OK;
+    }
+  } else if (use_decode_kernel(a)) {
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
     const int bn = decode_block_n(a->d);
@@ -551,6 +619,10 @@ fa_status fa_fwd_splitkv(const fa_fwd_args* a, int32_t num_splits, void* workspa
     if (e != cudaSuccess) return FA_ERR_CUDA;
     if (splits_used) *splits_used = ns;
     return FA_OK;  // the decode kernel merges the splits itself
+  } else if (ns == 1) {
+    // one split is the plain forward (the kernel writes O and LSE itself)
+    if (splits_used) *splits_used = 1;
+    return fa_fwd(a, stream);
   } else {
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
