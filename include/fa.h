@@ -140,10 +140,14 @@ size_t fa_splitkv_workspace_size(const fa_fwd_args* args, int32_t num_splits);
  * contiguous ranges of ceil(nblk / num_splits) blocks; split s writes its
  * normalised partial O_s and LSE_s into the workspace (0 and -inf for a split
  * with no visible key), then they are merged into args->o and args->lse as
- * fa_splitkv_combine does: for sq > 1 by that kernel, for sq == 1 inside the
- * split kernel (the last split of each head group to finish merges them; one
- * launch plus a small memset of the counters).  For sq == 1 the query heads
- * sharing a KV head are folded into one CTA (section 7.4).  num_splits == 0 picks the count with the heuristic;
+ * fa_splitkv_combine does.  With one split the kernel writes O and LSE itself.
+ * For sq == 1 the g = hq / hkv query heads sharing a KV head are folded
+ * together (section 7.4): for g >= 8 without a sliding window they become the
+ * rows of one tensor-core query tile (Q viewed as [b][g][hkv][d]; merged by
+ * the combine kernel); otherwise up to four of them share a CUDA-core CTA and
+ * the last split of each head group to finish merges the partials inside the
+ * split kernel (one launch plus a small memset of the counters).
+ * num_splits == 0 picks the count with the heuristic;
  * the count used is written to *splits_used (may be NULL).  The workspace is a
  * caller-owned device buffer of at least fa_splitkv_workspace_size bytes,
  * 256-byte aligned, needing no initialisation; two calls whose work overlaps on
