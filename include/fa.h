@@ -227,9 +227,15 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits
  * same split kernel and LSE-weighted combine as fa_fwd_splitkv, with the key
  * blocks of each sequence addressed through its block table or its prefix sum
  * and cut into num_splits ranges of that sequence's own length (0 = the
- * split-count heuristic, applied with max_seqlen_k), merged inside the split
- * kernel as for fa_fwd_splitkv with sq == 1.  The workspace is caller-owned device memory of at least
- * fa_kvcache_workspace_size bytes, 256-byte aligned, under the same rules as fa_fwd_splitkv's.
+ * split-count heuristic, applied with max_seqlen_k) and merged as for
+ * fa_fwd_splitkv with sq == 1: with g = hq / hkv >= 8 query heads per KV head
+ * and no window, the g heads are the rows of one tensor-core tile whose K/V
+ * blocks are loaded page by page (the V rows of a sequence's last block that
+ * lie past its end are zeroed in shared memory before they are multiplied, so
+ * whatever the cache holds there never reaches O); otherwise the CUDA-core
+ * kernel merges the splits itself.  The workspace is caller-owned device memory
+ * of at least fa_kvcache_workspace_size bytes, 256-byte aligned, under the same
+ * rules as fa_fwd_splitkv's.
  */
 fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
                          int32_t* splits_used, void* stream);

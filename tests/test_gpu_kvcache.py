@@ -63,6 +63,15 @@ PAGED = [
     (2, 8, 2, 128, "bf16", 192, [1000, 385], 0),
     (3, 4, 2, 64, "fp16", 64, [300, 129, 64], 2),
     (2, 8, 2, 128, "bf16", 320, [641, 1279], 3),
+    # g = hq / hkv >= 8: the heads of a KV head are the rows of one tensor-core
+    # tile (one and two 128-row tiles; 64-row boxes from different pages)
+    (3, 16, 2, 128, "bf16", 64, [1, 777, 5000], 0),
+    (3, 32, 2, 128, "fp16", 256, [300, 0, 4100], 3),
+    (2, 64, 8, 128, "bf16", 128, [2049, 6000], 1),
+    (2, 16, 1, 64, "bf16", 192, [1000, 385], 0),
+    (2, 128, 1, 128, "bf16", 320, [641, 1279], 3),
+    (1, 256, 1, 128, "bf16", 128, [3000], 0),
+    (2, 16, 2, 256, "fp16", 128, [700, 2], 2),
 ]
 
 
@@ -105,6 +114,9 @@ PACKED = [
     (4, 8, 2, 128, "bf16", [5, 1000, 0, 1995], 0),
     (3, 16, 4, 128, "fp16", [4096, 63, 65], 4),
     (2, 4, 1, 64, "bf16", [1, 300], 1),
+    (4, 16, 2, 128, "bf16", [5, 1000, 0, 1995], 0),
+    (2, 64, 4, 64, "fp16", [4096, 63], 4),
+    (2, 8, 1, 128, "bf16", [130, 1], 1),
 ]
 
 

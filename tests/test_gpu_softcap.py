@@ -105,12 +105,13 @@ def test_decode_softcap(case):
     _compare_all(q, k, v, False, None, None, c, o, lse, f"decode {case}")
 
 
+@pytest.mark.parametrize("hq", [8, 32])
 @pytest.mark.parametrize("paged", [True, False])
-def test_kvcache_softcap(paged):
-    b, hq, hkv, d, ps, c = 3, 8, 2, 128, 128, 5.0
+def test_kvcache_softcap(paged, hq):
+    b, hkv, d, ps, c = 3, 2, 128, 128, 5.0
     lens = [1, 700, 2345]
     dt = torch.bfloat16
-    seed = 2718 + int(paged)
+    seed = 2718 + int(paged) + hq
     q = normal((b, hq, d), seed, 1, STD, dt)
     ks = [normal((n, hkv, d), seed, 10 + 2 * i, STD, dt) for i, n in enumerate(lens)]
     vs = [normal((n, hkv, d), seed, 11 + 2 * i, 1.0, dt) for i, n in enumerate(lens)]
@@ -145,7 +146,7 @@ def test_kvcache_softcap(paged):
                                   softcap=c)
         o_ref[i], l_ref[i] = oi, li
     assert_parity(o.to(torch.float64).cpu().numpy().reshape(-1, d), lse.cpu().double().numpy().reshape(-1),
-                  o_ref.reshape(-1, d), l_ref.reshape(-1), dt, f"kvcache softcap paged={paged}")
+                  o_ref.reshape(-1, d), l_ref.reshape(-1), dt, f"kvcache softcap paged={paged} hq={hq}")
 
 
 def test_varlen_softcap():

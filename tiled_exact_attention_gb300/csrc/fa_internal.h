@@ -46,6 +46,16 @@ struct PrefillParams {
   // Softcap (sc_b > 0): the raw score x = q.k becomes, in log2 units,
   // sc_b * tanh(s / c) with tanh(s / c) = 1 - 2 / (2^(sc_k x) + 1); sc_b = c log2(e).
   float sc_k, sc_b;
+  // KV cache (kv_mode = kKvPaged or kKvPacked; the packed-sequence kernels): Q
+  // stays dense ([b][sq][hq][d] through tm_q, batch coordinate b); sequence b has
+  // seqlens[b] keys in pages of block_table (tm_k / tm_v over [pages][page_size]
+  // [hkv][d], boxes of box_rows keys that never straddle a page) or the keys
+  // [cu_k[b], cu_k[b + 1]) (tm_k / tm_v over [total_k][hkv][d]); no mask edges,
+  // split mode always, each sequence cut into num_splits ranges of its own length.
+  int kv_mode;
+  const int* block_table;
+  int bt_stride, page_size, box_rows;
+  const int* seqlens;
 };
 
 // Where the decode kernel finds a sequence's keys.

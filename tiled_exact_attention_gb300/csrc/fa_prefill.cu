@@ -90,7 +90,8 @@ template <int NQ>
 struct ItemPlan {
   int bi, h, kvh, m_cta, split;
   int sq, skv, off, left_off;  // the sequence's sizes and mask edges
-  int q_base, k_base, tb;      // packed row offsets; batch coordinate of the tensor maps
+  int q_base, k_base, tb;      // packed row offsets; batch coordinate of the Q map
+  int tbk;                     // batch coordinate of the K/V maps (a KV cache's pages: per block)
   int n_hi[NQ], n_lo_t[NQ];    // tile t visits key blocks [n_lo_t[t], n_hi[t])
   int n_hi_max;                // the CTA streams blocks n_hi_max - 1 down to n_hi_max - N
   int N;
@@ -119,8 +120,19 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   w.q_base = 0;
   w.k_base = 0;
   w.tb = w.bi;
+  w.tbk = w.bi;
   w.valid = true;
-  if constexpr (VARLEN) {
+  if (VARLEN && p.kv_mode != kKvDense) {
+    // KV cache: dense Q; the sequence's own keys, paged or packed (clamped
+    // lengths; a page or row outside the cache reads as zeros, never faults)
+    w.tbk = 0;
+    if (p.kv_mode == kKvPaged) {
+      w.skv = max(p.seqlens[w.bi], 0);
+    } else {
+      w.k_base = p.cu_k[w.bi];
+      w.skv = max(p.cu_k[w.bi + 1] - w.k_base, 0);
+    }
+  } else if constexpr (VARLEN) {
     // Packed: sequence bi owns Q rows [cu_q[bi], cu_q[bi + 1]) and K/V rows
     // [cu_k[bi], cu_k[bi + 1]); its mask edges sit on its own bottom-right
     // diagonal (the host passes them relative to that diagonal).
@@ -129,6 +141,7 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
     w.k_base = p.cu_k[w.bi];
     w.skv = p.cu_k[w.bi + 1] - w.k_base;
     w.tb = 0;
+    w.tbk = 0;
     w.valid = w.q_base >= 0 && w.sq >= 0 && w.q_base <= p.total_q - w.sq && w.k_base >= 0 && w.skv >= 0 &&
               w.k_base <= p.total_k - w.skv && w.sq <= p.n_mtiles * BM;
     if (!w.valid) {
@@ -143,8 +156,11 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   const int nblk_total = (w.skv + BN - 1) / BN;
   int n_lo = 0, n_cap = nblk_total;
   if (p.num_splits > 1) {
-    n_lo = w.split * p.blocks_per_split;
-    n_cap = min(nblk_total, n_lo + p.blocks_per_split);
+    // (a KV cache cuts every sequence into num_splits ranges of its own length)
+    const int bps =
+        VARLEN && p.kv_mode != kKvDense ? max(1, (nblk_total + p.num_splits - 1) / p.num_splits) : p.blocks_per_split;
+    n_lo = w.split * bps;
+    n_cap = min(nblk_total, n_lo + bps);
     if (n_lo > n_cap) n_lo = n_cap;
   }
   // The union of the tiles' ranges is contiguous: the tiles are adjacent rows.
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             const int m_cta = p.n_mcta - 1 - idx / (p.b * p.hq);
             const int bi = bh / p.hq, h = bh % p.hq;
             int base = 0, rows = p.sq, tb = bi;
-            if constexpr (VARLEN) {  // (offsets are range-checked when the item itself is planned)
+            if (VARLEN && p.kv_mode == kKvDense) {  // (offsets are range-checked when the item itself is planned)
               base = p.cu_q[bi];
               rows = min(p.cu_q[bi + 1] - base, p.n_mtiles * BM);
               tb = 0;
@@ -330,14 +346,30 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
           mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
           if (E8 && (L & 1)) {
             // V transposed ([d rows][keys]): one box of D rows x BN keys
-            tma_load_4d_hint(ring + slot * C::KV_BYTES, &p.tm_v, &kv_full[slot], w.k_base + n * BN, 0, w.kvh, w.tb,
+            tma_load_4d_hint(ring + slot * C::KV_BYTES, &p.tm_v, &kv_full[slot], w.k_base + n * BN, 0, w.kvh, w.tbk,
                              pol_kv);
+          } else if (VARLEN && p.kv_mode == kKvPaged) {
+            // paged cache: box_rows keys per box (BN, or 64 when a page holds no
+            // whole block), each from its page; a box past the sequence's end
+            // (rows masked) reuses the block's first page
+            const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
+            const int* bt_row = p.block_table + static_cast<int64_t>(w.bi) * p.bt_stride;
+            const int r0 = n * BN;
+            const int pg0 = bt_row[r0 / p.page_size];
+            for (int sb = 0; sb * p.box_rows < BN; ++sb) {
+              const int r = r0 + sb * p.box_rows;
+              const int pg = (sb == 0 || r >= w.skv) ? pg0 : bt_row[r / p.page_size];
+#pragma unroll
+              for (int c = 0; c < C::DC; ++c)
+                tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128) + sb * p.box_rows * 128, map,
+                                 &kv_full[slot], c * C::CHUNK_ELEMS, w.kvh, r % p.page_size, pg, pol_kv);
+            }
           } else {
             const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
 #pragma unroll
             for (int c = 0; c < C::DC; ++c)
               tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * C::CHUNK_ELEMS,
-                               w.kvh, w.k_base + n * BN, w.tb, pol_kv);
+                               w.kvh, w.k_base + n * BN, w.tbk, pol_kv);
           }
         }
       }
@@ -462,8 +494,9 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
     const uint32_t tS = tbase + lane_off + C::s_col(t);
     const uint32_t tO = tbase + lane_off + C::o_col(t);
     const float sl2 = p.scale_log2;
-    const bool split_mode = p.num_splits > 1;
+    const bool split_mode = p.o_part != nullptr;
     uint32_t gblk = 0;  // key blocks this tile has processed, over all items
+    uint32_t g_loads = 0;  // K/V loads of the items before this one (the producer's count)
     bool ok = true;
     for (int j = 0; ok; ++j) {
       const int item = item_of(j);
@@ -473,12 +506,35 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       const float* kd = nullptr;  // e4m3: the K scales of this head's key blocks
       {
         const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+        const uint32_t first_load = g_loads;
+        g_loads += 2 * w.N;
         if (VARLEN && !w.valid) {
           if (threadIdx.x == 0) record_error(p.status, kErrDeviceArg);
           continue;
         }
         row0 = (w.m_cta * NQ + t) * BM;
         if (row0 >= w.sq) continue;  // no row of this tile in the sequence
+        if (VARLEN && p.kv_mode != kKvDense && t == 0 && w.N > 0 && w.skv - (w.n_hi_max - 1) * BN < BN) {
+          // KV cache: rows past a sequence's end may hold anything (NaN too) and
+          // 0 * NaN is NaN in P V, so tile 0's threads zero the V rows of the
+          // block that ends the sequence (the item's first) before its P is
+          // released: generic stores, then the proxy fence that orders them
+          // before the tensor core's reads; the slot is not refilled before that
+          // PV has completed.
+          const int v_zero = w.skv - (w.n_hi_max - 1) * BN;
+          const uint32_t v_load = first_load + 1, slot = v_load % C::STAGES;
+          if (!warp_wait(&kv_full[slot], (v_load / C::STAGES) & 1, p.status, kSiteKvFull)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vs = ring + slot * C::KV_BYTES;
+          const int units = (BN - v_zero) * C::DC * 8;  // 16-byte units
+          for (int u = r; u < units; u += BM) {
+            const int row = v_zero + u / (C::DC * 8), c = (u >> 3) % C::DC;
+            *reinterpret_cast<uint4*>(vs + c * (BN * 128) + row * 128 + (u & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
         if constexpr (E8) {  // (the tile exists: its scale index is below n_mtiles)
           sl2q = sl2 * p.q_descale[(static_cast<int64_t>(w.bi) * p.hq + w.h) * p.n_mtiles + w.m_cta * NQ + t];
           kd = p.k_descale + (static_cast<int64_t>(w.bi) * p.hkv + w.kvh) * p.n_kblocks;
@@ -742,9 +798,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = p.sc_b > 0.f ? (p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true, false, true>
-                                                : fa_prefill_kernel<D, BF16, false, false, true>)
-                           : (p.cu_q != nullptr ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>);
+  const bool varlen = p.cu_q != nullptr || p.kv_mode != kKvDense;
+  auto kern = p.sc_b > 0.f ? (varlen ? fa_prefill_kernel<D, BF16, true, false, true>
+                                     : fa_prefill_kernel<D, BF16, false, false, true>)
+                           : (varlen ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;
