@@ -98,7 +98,7 @@ struct ItemPlan {
   bool valid;                  // false: packed offsets out of range (nothing is touched)
 };
 
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, bool CACHE>
 __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p, int item) {
   using C = Cfg<D>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
@@ -122,7 +122,7 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   w.tb = w.bi;
   w.tbk = w.bi;
   w.valid = true;
-  if (VARLEN && p.kv_mode != kKvDense) {
+  if constexpr (CACHE) {
     // KV cache: dense Q; the sequence's own keys, paged or packed (clamped
     // lengths; a page or row outside the cache reads as zeros, never faults)
     w.tbk = 0;
@@ -158,7 +158,7 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   if (p.num_splits > 1) {
     // (a KV cache cuts every sequence into num_splits ranges of its own length)
     const int bps =
-        VARLEN && p.kv_mode != kKvDense ? max(1, (nblk_total + p.num_splits - 1) / p.num_splits) : p.blocks_per_split;
+        CACHE ? max(1, (nblk_total + p.num_splits - 1) / p.num_splits) : p.blocks_per_split;
     n_lo = w.split * bps;
     n_cap = min(nblk_total, n_lo + bps);
     if (n_lo > n_cap) n_lo = n_cap;
@@ -216,6 +216,8 @@ __device__ __forceinline__ int item_of(int j) {
 
 // VARLEN: packed variable-length sequences (p.cu_q / p.cu_k); a separate
 // instantiation so that the dense kernel keeps its sizes in the constant bank.
+// CACHE (with VARLEN): a KV cache read with dense Q (p.kv_mode), again a
+// separate instantiation so that the packed-sequence kernel keeps its code.
 //
 // Persistent: one CTA per SM walks its items; the producer loads the next
 // item's Q as soon as the last S MMA of the current item has read Q, and the MMA
@@ -223,7 +225,7 @@ __device__ __forceinline__ int item_of(int j) {
 // item's output (its PV MMAs wait only until the previous O has been read out).
 // SC: softcap, each score capped to c tanh(s / c) before the mask (a separate
 // instantiation: two more special-function operations per score).
-template <int D, bool BF16, bool VARLEN, bool E8 = false, bool SC = false>
+template <int D, bool BF16, bool VARLEN, bool E8 = false, bool SC = false, bool CACHE = false>
 __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D, E8>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       for (int j = 0; ok; ++j) {
         const int item = item_of(j);
         if (item >= total_items) break;
-        const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
         if (w.N == 0) continue;
         // Q buffer free: the previous item's S MMAs have completed
         if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, p.status, kSiteQEmpty)) break;
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             const int m_cta = p.n_mcta - 1 - idx / (p.b * p.hq);
             const int bi = bh / p.hq, h = bh % p.hq;
             int base = 0, rows = p.sq, tb = bi;
-            if (VARLEN && p.kv_mode == kKvDense) {  // (offsets are range-checked when the item itself is planned)
+            if constexpr (VARLEN && !CACHE) {  // (offsets are range-checked when the item itself is planned)
               base = p.cu_q[bi];
               rows = min(p.cu_q[bi + 1] - base, p.n_mtiles * BM);
               tb = 0;
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             // V transposed ([d rows][keys]): one box of D rows x BN keys
             tma_load_4d_hint(ring + slot * C::KV_BYTES, &p.tm_v, &kv_full[slot], w.k_base + n * BN, 0, w.kvh, w.tbk,
                              pol_kv);
-          } else if (VARLEN && p.kv_mode == kKvPaged) {
+          } else if (CACHE && p.kv_mode == kKvPaged) {
             // paged cache: box_rows keys per box (BN, or 64 when a page holds no
             // whole block), each from its page; a box past the sequence's end
             // (rows masked) reuses the block's first page
@@ -401,7 +403,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         if (item >= total_items) break;
         int N, it_b[NQ], it_e[NQ];  // tile t is active in iterations [it_b[t], it_e[t])
         {
-          const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+          const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
           N = w.N;
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
@@ -505,16 +507,16 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       float sl2q = sl2;        // e4m3: the tile's Q scale folded into the score scale
       const float* kd = nullptr;  // e4m3: the K scales of this head's key blocks
       {
-        const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);
+        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
         const uint32_t first_load = g_loads;
-        g_loads += 2 * w.N;
+        if constexpr (CACHE) g_loads += 2 * w.N;
         if (VARLEN && !w.valid) {
           if (threadIdx.x == 0) record_error(p.status, kErrDeviceArg);
           continue;
         }
         row0 = (w.m_cta * NQ + t) * BM;
         if (row0 >= w.sq) continue;  // no row of this tile in the sequence
-        if (VARLEN && p.kv_mode != kKvDense && t == 0 && w.N > 0 && w.skv - (w.n_hi_max - 1) * BN < BN) {
+        if (CACHE && t == 0 && w.N > 0 && w.skv - (w.n_hi_max - 1) * BN < BN) {
           // KV cache: rows past a sequence's end may hold anything (NaN too) and
           // 0 * NaN is NaN in P V, so tile 0's threads zero the V rows of the
           // block that ends the sequence (the item's first) before its P is
@@ -690,7 +692,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       if (!ok) break;
 
       // ---------------- epilogue (overlaps the next item's first MMAs) ----------------
-      const ItemPlan<NQ> w = plan_item<D, VARLEN>(p, item);  // recomputed: fewer registers in the loop
+      const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);  // recomputed: fewer registers in the loop
       const bool valid = row < w.sq;
       // LSE [b][hq][sq], or [hq][total_q] for packed sequences
       const int64_t lse_idx = VARLEN ? static_cast<int64_t>(w.h) * p.total_q + w.q_base + row
@@ -798,10 +800,13 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
   using C = Cfg<D>;
-  const bool varlen = p.cu_q != nullptr || p.kv_mode != kKvDense;
-  auto kern = p.sc_b > 0.f ? (varlen ? fa_prefill_kernel<D, BF16, true, false, true>
-                                     : fa_prefill_kernel<D, BF16, false, false, true>)
-                           : (varlen ? fa_prefill_kernel<D, BF16, true> : fa_prefill_kernel<D, BF16, false>);
+  const bool sc = p.sc_b > 0.f;
+  auto kern = sc ? fa_prefill_kernel<D, BF16, false, false, true> : fa_prefill_kernel<D, BF16, false>;
+  if (p.kv_mode != kKvDense)
+    kern = sc ? fa_prefill_kernel<D, BF16, true, false, true, true>
+              : fa_prefill_kernel<D, BF16, true, false, false, true>;
+  else if (p.cu_q != nullptr)
+    kern = sc ? fa_prefill_kernel<D, BF16, true, false, true> : fa_prefill_kernel<D, BF16, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq * p.num_splits;
