@@ -443,7 +443,9 @@ def bench_variants(dev, flush, pk, steps=20):
     visible (query, key) pairs (4 d flops per pair and head), against the sustained bf16 peak:
       * window: the causal prefill workload with a sliding window of 1024 keys (local causal);
       * softcap: the causal prefill workload with every score capped to 30 tanh(s / 30);
-      * varlen: 16 packed causal sequences, lengths drawn (seeded) from [256, 4096], H = 16, d = 128."""
+      * varlen: 16 packed causal sequences, lengths drawn (seeded) from [256, 4096], H = 16, d = 128;
+      * decode_g8: split-KV decode with 8 query heads per KV head (B = 8, Hq = 64, Hkv = 8, KV = 32768,
+        d = 128), whose heads are the rows of one tensor-core tile; KV GB/s against the measured copy peak."""
     import numpy as np
     import torch
 
@@ -491,6 +493,26 @@ def bench_variants(dev, flush, pk, steps=20):
                                 "causal": True},
                      "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
                                   "frac": round(tf / pk, 4), "traffic": None}}
+    from tiled_exact_attention_gb300 import fa_fwd_splitkv
+    from tiled_exact_attention_gb300.api import fa_splitkv_workspace_size
+    from tiled_exact_attention_gb300.inputs import make_custom
+
+    del qv, kv, vv, ov, lv
+    b, skv, hq, hkv, d = 8, 32768, 64, 8, 128
+    qd, kd, vd = (t.to(dev) for t in make_custom(b, 1, skv, hq, hkv, d, "bf16", seed=BASE_SEED + 70))
+    od = torch.empty_like(qd)
+    ld = torch.empty((b, hq, 1), dtype=torch.float32, device=dev)
+    work = torch.empty(fa_splitkv_workspace_size(qd, kd, vd, 0), dtype=torch.uint8, device=dev)
+    used = fa_fwd_splitkv(qd, kd, vd, workspace=work, out=od, lse=ld, return_splits=True)[2]
+    ms = _timed(lambda: fa_fwd_splitkv(qd, kd, vd, workspace=work, out=od, lse=ld), flush, steps)
+    nbytes = 2 * b * skv * hkv * d * 2 + 2 * b * hq * d * 2 + b * hq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = float(_peaks()[0]["hbm_gbs"])
+    out["decode_g8"] = {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                        "config": {"b": b, "skv": skv, "hq": hq, "hkv": hkv, "d": d, "num_splits": used,
+                                   "kernels": "fa_prefill_kernel (heads as rows) + fa_combine_kernel"},
+                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                     "frac": round(gbs / hbm, 4), "traffic": None}}
     if fa_sync_status() != 0:
         raise RuntimeError("device status set by a forward-pass variant")
     return out
