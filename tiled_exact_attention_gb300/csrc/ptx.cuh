@@ -261,48 +261,50 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05: MMA issue (one thread)
+// tcgen05: MMA issue.  W = false: one thread issues (the others of its warp do
+// not take part).  W = true: the whole warp, converged, executes the call and
+// one lane chosen by elect.sync issues; kept warp-uniform this way, the issue
+// returns at once instead of holding the issuing thread for about the MMA's own
+// execution time (measured ~61 vs ~2 cycles per MMA into an empty pipe), so the
+// issuer runs ahead of the tensor pipe.
 // ---------------------------------------------------------------------------
+#define FA_UMMA(W, INSTR, A_CONSTRAINT)                                                                       \
+  if constexpr (W)                                                                                            \
+    asm volatile("{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t@e " INSTR \
+                 "\n\t}" ::"r"(d_tmem), A_CONSTRAINT(a), "l"(b_desc), "r"(idesc), "r"(accumulate));                  \
+  else                                                                                                        \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t" INSTR "\n\t}" ::"r"(d_tmem), A_CONSTRAINT(a),  \
+                 "l"(b_desc), "r"(idesc), "r"(accumulate))
+
 // D[tmem] (+)= A[smem] * B[smem].  No memory clobber: MMAs touch no memory the
 // compiler tracks, and volatile asm keeps their order relative to the commits
 // and barrier operations around them.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+template <bool W = false>
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+  FA_UMMA(W, "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;", "l");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+template <bool W = false>
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+  FA_UMMA(W, "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;", "r");
 }
 
 // The same two forms with 8-bit operands (kind::f8f6f4, K = 32 per instruction).
-__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+template <bool W = false>
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+  FA_UMMA(W, "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;", "l");
 }
 
-__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+template <bool W = false>
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+  FA_UMMA(W, "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;", "r");
 }
+#undef FA_UMMA
 
 // Instruction descriptor, kind::f8f6f4: D f32, A and B e4m3 (format 0), both K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
@@ -319,11 +321,18 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
-// has completed.
+// has completed (W: the converged warp executes it, the elected lane commits).
+template <bool W = false>
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
+  if constexpr (W)
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -14,8 +14,9 @@ __device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b :
 
 // A bounded wait whose outcome is the same on every lane of the warp, so that the
 // warp stays converged for the warp-collective TMEM instructions that follow.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int site) {
-  const bool ok = mbar_wait(bar, parity, status, site);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int site,
+                                          uint32_t sleep_ns = 0) {
+  const bool ok = mbar_wait(bar, parity, status, site, false, sleep_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -90,7 +91,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // S_t = Q_t K^T over the head dimension: D / 16 MMAs of K = 16, both operands
 // K-major with 128-byte swizzle (64-column chunks of 128-byte rows).
-template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID>
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool W = false>
 __device__ __forceinline__ void issue_s_tile(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int t, int slot) {
   uint64_t qd = q_desc + static_cast<uint32_t>((t * Q_BYTES) >> 4);
   uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
@@ -101,27 +102,27 @@ __device__ __forceinline__ void issue_s_tile(uint32_t d_tmem, uint64_t q_desc, u
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
     const uint32_t offb = static_cast<uint32_t>(((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4);
-    umma_ss(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
+    umma_ss<W>(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
   }
 }
 
 // O_t (+)= P_t[:, 16 k0 : 16 k1] V[16 k0 : 16 k1, :]: P from TMEM (two 16-bit
 // values per column), V MN-major with 128-byte swizzle (64-column atoms BN * 128
 // bytes apart, 8-row groups 1024 bytes apart).
-template <int D, int BN, int KV_BYTES, uint32_t ID, int K0, int K1>
+template <int D, int BN, int KV_BYTES, uint32_t ID, int K0, int K1, bool W = false>
 __device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, int slot, bool acc) {
   uint64_t vd = v_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
   asm volatile("" : "+l"(vd));
 #pragma unroll
   for (int k = K0; k < K1; ++k) {
-    umma_ts(o_tmem, p_tmem + k * 8, vd + static_cast<uint32_t>((k * 2048) >> 4), ID, (acc || k > 0) ? 1u : 0u);
+    umma_ts<W>(o_tmem, p_tmem + k * 8, vd + static_cast<uint32_t>((k * 2048) >> 4), ID, (acc || k > 0) ? 1u : 0u);
   }
 }
 
 
 // 8-bit forms: S = Q K^T with e4m3 operands (D / 32 MMAs of K = 32, same 128-byte
 // swizzled K-major layout: a 128-byte row holds 128 elements) ...
-template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID>
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool W = false>
 __device__ __forceinline__ void issue_s_tile_e4m3(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int q_slot,
                                                   int slot) {
   uint64_t qd = q_desc + static_cast<uint32_t>((q_slot * Q_BYTES) >> 4);
@@ -131,14 +132,14 @@ __device__ __forceinline__ void issue_s_tile_e4m3(uint32_t d_tmem, uint64_t q_de
   for (int k = 0; k < D / 32; ++k) {
     const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
     const uint32_t offb = static_cast<uint32_t>(((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4);
-    umma_ss_f8(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
+    umma_ss_f8<W>(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
   }
 }
 
 // ... and O (+)= P V with P e4m3 in TMEM (four per column, K = 32 per MMA = 8
 // columns) and V stored transposed ([d rows][keys], K-major, one 128-byte chunk of
 // BN = 128 keys per row).
-template <int D, int BN, int KV_BYTES, uint32_t ID>
+template <int D, int BN, int KV_BYTES, uint32_t ID, bool W = false>
 __device__ __forceinline__ void issue_pv_tile_e4m3(uint32_t o_tmem, uint32_t p_tmem, uint64_t vt_desc, int slot,
                                                    bool acc) {
   uint64_t vd = vt_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
@@ -146,7 +147,7 @@ __device__ __forceinline__ void issue_pv_tile_e4m3(uint32_t o_tmem, uint32_t p_t
 #pragma unroll
   for (int k = 0; k < BN / 32; ++k) {
     const uint32_t off = static_cast<uint32_t>(((k >> 2) * (D * 128) + (k & 3) * 32) >> 4);
-    umma_ts_f8(o_tmem, p_tmem + k * 8, vd + off, ID, (acc || k > 0) ? 1u : 0u);
+    umma_ts_f8<W>(o_tmem, p_tmem + k * 8, vd + off, ID, (acc || k > 0) ? 1u : 0u);
   }
 }
 
