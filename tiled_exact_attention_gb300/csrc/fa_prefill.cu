@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
               tc_fence_after();
               issue_pv<D, BN, C::KV_BYTES, kIdO, E8, WI>(tbase + C::o_col(t), tbase + C::s_col(t), v_desc,
                                                                  Lv % C::STAGES, !first);
-              umma_commit<WI>(&o_full[t]);
+              if (it + 1 == it_e[t]) umma_commit<WI>(&o_full[t]);  // the tile's last PV of the item
               ++pv_cnt[t];
             }
             if (has_next && FA_ACTIVE(t, it + 1)) {
@@ -514,6 +514,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
     const float sl2 = p.scale_log2;
     const bool split_mode = p.o_part != nullptr;
     uint32_t gblk = 0;  // key blocks this tile has processed, over all items
+    uint32_t oitems = 0;  // items whose O this tile has read out (o_full completes once per item)
     uint32_t g_loads = 0;  // K/V loads of the items before this one (the producer's count)
     bool ok = true;
     for (int j = 0; ok; ++j) {
@@ -583,15 +584,6 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
           break;
         }
         tc_fence_after();
-        if (k > 0) {
-          // S_k complete implies PV_{k-1} complete; observe that phase of o_full so
-          // the final wait below is never more than one phase behind.
-          if (!warp_wait(&o_full[t], (gblk - 1) & 1, p.status, kSiteOFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         uint32_t sr[BN];
         tmem_load_row<BN>(tS, sr);
         float* s = reinterpret_cast<float*>(sr);
@@ -631,9 +623,11 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         const bool grow = bm2 > m_run + kRescaleLog2;
         const float m_new = grow ? bm2 : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
+        float alpha = 1.f;  // (l_run is 0 before the first block: alpha is not needed there)
         if (k > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_t already holds the previous blocks' product (see the o_full wait).
+          alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
+          // O_t already holds the previous blocks' product: S_k complete implies
+          // PV_{k-1} complete (one issuing thread, in-order completion).
           // 32 columns at a time: the 128 scores are still live in registers.
           constexpr int CH = 32;
 #pragma unroll
@@ -733,10 +727,11 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         }
         continue;
       }
-      if (!warp_wait(&o_full[t], (gblk - 1) & 1, p.status, kSiteOFull)) {
+      if (!warp_wait(&o_full[t], oitems & 1, p.status, kSiteOFull)) {
         ok = false;
         break;
       }
+      ++oitems;
       tc_fence_after();
       // (e4m3: the V scale of the head applies to the whole accumulator)
       const float vscale = E8 ? p.v_descale[static_cast<int64_t>(w.bi) * p.hkv + w.kvh] : 1.f;
