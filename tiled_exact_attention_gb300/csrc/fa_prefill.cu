@@ -55,7 +55,7 @@ struct Cfg {
   static constexpr int O_COL0 = 256;
   static constexpr int RING_OFF = NQ * Q_BYTES;
   static constexpr int BAR_OFF = RING_OFF + STAGES * KV_BYTES;
-  static constexpr int NUM_BARS = 3 + 4 * NQ + 2 * STAGES;
+  static constexpr int NUM_BARS = 3 + 5 * NQ + 2 * STAGES;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;
   // Register split (NQ == 2): launched at 168 per thread (384 threads), the
   // control warpgroup drops to 72 and the two softmax warpgroups rise to 216:
@@ -240,6 +240,10 @@ template <int D, bool BF16, bool VARLEN, bool E8 = false, bool SC = false, bool 
 __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = Cfg<D, E8>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
+  // P released in two halves of the block's keys (the first half's PV runs while
+  // the second is formed): measured faster for d = 64 (+6%), d = 256 (+5%) and
+  // softcap (+2%), slower for d = 128 (-3%, long GQA -7%)
+  constexpr bool HALF_P = !E8 && (D != 128 || SC);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -253,7 +257,8 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
   uint64_t* o_full = p_full + NQ;
   uint64_t* o_empty = o_full + NQ;
   uint64_t* mma_done = o_empty + NQ;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* p_half = mma_done + 1;  // P of the block's first half of keys written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + NQ);
   uint8_t* ring = smem + C::RING_OFF;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,6 +273,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
     for (int t = 0; t < NQ; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], BM);
+      mbar_init(&p_half[t], BM);
       mbar_init(&o_full[t], 1);
       mbar_init(&o_empty[t], BM);
     }
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
             if (FA_ACTIVE(t, it)) {
-              if (!issuer_wait<WI>(&p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
+              if (!issuer_wait<WI>(HALF_P ? &p_half[t] : &p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
                 ok = false;
                 break;
               }
@@ -465,8 +471,21 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
                 break;
               }
               tc_fence_after();
-              issue_pv<D, BN, C::KV_BYTES, kIdO, E8, WI>(tbase + C::o_col(t), tbase + C::s_col(t), v_desc,
-                                                                 Lv % C::STAGES, !first);
+              if constexpr (!HALF_P) {
+                issue_pv<D, BN, C::KV_BYTES, kIdO, E8, WI>(tbase + C::o_col(t), tbase + C::s_col(t), v_desc,
+                                                           Lv % C::STAGES, !first);
+              } else {
+                // the block's first 64 keys as soon as their P is written, then the rest
+                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 32, WI>(tbase + C::o_col(t), tbase + C::s_col(t),
+                                                                       v_desc, Lv % C::STAGES, !first);
+                if (!issuer_wait<WI>(&p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, BN / 32, BN / 16, WI>(tbase + C::o_col(t), tbase + C::s_col(t),
+                                                                             v_desc, Lv % C::STAGES, true);
+              }
               if (it + 1 == it_e[t]) umma_commit<WI>(&o_full[t]);  // the tile's last PV of the item
               ++pv_cnt[t];
             }
@@ -688,10 +707,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 #pragma unroll
           for (int c = 0; c < BN / 4; c += 16)
             tmem_st16(tS + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
-          if (half == 1) {
+          if (HALF_P || half == 1) {
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[t]);
+            mbar_arrive(half == 0 ? &p_half[t] : &p_full[t]);
           }
         }
         }
