@@ -94,6 +94,10 @@ DECODE = [
     (3, 3000, 4, 4, 64, "fp16", (300, -1), 0),
     (1, 2000, 8, 1, 256, "bf16", (0, 0), 0),
     (2, 700, 8, 2, 128, "bf16", (63, 0), 3),
+    # g = 16: a window keeps the CUDA-core decode kernel; one wider than the keys is
+    # dropped and the heads-as-rows tile takes the call
+    (2, 3000, 32, 2, 128, "bf16", (500, 0), 0),
+    (1, 1000, 16, 2, 128, "bf16", (5000, 0), 0),
 ]
 
 

@@ -403,6 +403,60 @@ int resolve_splits(const fa_fwd_args* a, int32_t requested, const DeviceInfo& di
 
 using namespace fa;
 
+// KV-cache decode with the heads as rows: Q [b][hq][d] viewed as [b][g][hkv][d]
+// (as in fa_fwd_splitkv), the cache read through the prefill kernel's paged or
+// packed K/V loads, split partials merged by the combine kernel.
+static fa_status kvcache_head_rows_run(const fa_kvcache_args* a, int ns, float* o_part, float* lse_part,
+                                       const DeviceInfo& di, int32_t* splits_used, void* stream) {
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int g = a->hq / a->hkv;
+  const int bn = prefill_block_n(a->d);
+  const bool paged = a->page_size > 0;
+  const int64_t q_view[3] = {a->q_strides[0], a->q_strides[1], static_cast<int64_t>(g) * a->q_strides[1]};
+  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hkv, g, a->b, q_view, 64, 128, true)) return FA_ERR_INVALID_ARG;
+  // 4-D views (d, hkv, rows, outer): paged rows = page_size, outer = pages; packed rows = total_k, outer = 1
+  const int64_t k_st[3] = {paged ? a->k_strides[0] : a->k_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
+                           a->k_strides[1], a->k_strides[2]};
+  const int64_t v_st[3] = {paged ? a->v_strides[0] : a->v_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
+                           a->v_strides[1], a->v_strides[2]};
+  const int rows_dim = paged ? a->page_size : a->num_pages;
+  const int outer_dim = paged ? a->num_pages : 1;
+  const int box_rows = (!paged || a->page_size % bn == 0) ? bn : 64;
+  if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, rows_dim, outer_dim, k_st, 64, box_rows, true) ||
+      !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, rows_dim, outer_dim, v_st, 64, box_rows, true))
+    return FA_ERR_INVALID_ARG;
+  p.lse = lse_part;  // partials [ns][b][hkv][g] = [ns][b][hq]
+  p.o_part = o_part;
+  p.b = a->b;
+  p.sq = g;
+  p.skv = a->max_seqlen_k;
+  p.hq = a->hkv;
+  p.hkv = a->hkv;
+  p.g = 1;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
+  p.n_mtiles = static_cast<int>(ceil_div64(g, 128));
+  p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
+  p.num_splits = ns;
+  p.blocks_per_split = 1;  // set per sequence in the kernel
+  p.max_ctas = di.sms;
+  p.status = di.status;
+  p.cu_k = paged ? nullptr : a->cu_seqlens_k;
+  p.total_k = a->num_pages;
+  p.kv_mode = paged ? kKvPaged : kKvPacked;
+  p.block_table = a->block_table;
+  p.bt_stride = a->block_table_stride;
+  p.page_size = a->page_size;
+  p.box_rows = box_rows;
+  p.seqlens = a->seqlens_k;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_prefill(p, a->d, a->dtype, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (splits_used) *splits_used = ns;
+  const int64_t o_st[3] = {a->o_strides[0], a->o_strides[1], a->o_strides[1]};  // (one row: its stride is unused)
+  return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, 1, a->d, a->dtype, a->o, o_st, a->lse, stream);
+}
+
 extern "C" {
 
 int32_t fa_version(void) { return 3; }
@@ -692,60 +746,6 @@ fa_status fa_fwd_splitkv_noalloc(const fa_fwd_args* a, int32_t num_splits, int32
   void* scratch = nullptr;
   if (!noalloc_scratch(&scratch)) return FA_ERR_CUDA;
   return fa_fwd_splitkv(a, num_splits, scratch, FA_NOALLOC_SCRATCH_BYTES, splits_used, stream);
-}
-
-// KV-cache decode with the heads as rows: Q [b][hq][d] viewed as [b][g][hkv][d]
-// (as in fa_fwd_splitkv), the cache read through the prefill kernel's paged or
-// packed K/V loads, split partials merged by the combine kernel.
-static fa_status kvcache_head_rows_run(const fa_kvcache_args* a, int ns, float* o_part, float* lse_part,
-                                       const DeviceInfo& di, int32_t* splits_used, void* stream) {
-  PrefillParams p;
-  std::memset(&p, 0, sizeof(p));
-  const int g = a->hq / a->hkv;
-  const int bn = prefill_block_n(a->d);
-  const bool paged = a->page_size > 0;
-  const int64_t q_view[3] = {a->q_strides[0], a->q_strides[1], static_cast<int64_t>(g) * a->q_strides[1]};
-  if (!encode_map(&p.tm_q, a->q, a->dtype, a->d, a->hkv, g, a->b, q_view, 64, 128, true)) return FA_ERR_INVALID_ARG;
-  // 4-D views (d, hkv, rows, outer): paged rows = page_size, outer = pages; packed rows = total_k, outer = 1
-  const int64_t k_st[3] = {paged ? a->k_strides[0] : a->k_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
-                           a->k_strides[1], a->k_strides[2]};
-  const int64_t v_st[3] = {paged ? a->v_strides[0] : a->v_strides[1] * (a->num_pages > 0 ? a->num_pages : 1),
-                           a->v_strides[1], a->v_strides[2]};
-  const int rows_dim = paged ? a->page_size : a->num_pages;
-  const int outer_dim = paged ? a->num_pages : 1;
-  const int box_rows = (!paged || a->page_size % bn == 0) ? bn : 64;
-  if (!encode_map(&p.tm_k, a->k, a->dtype, a->d, a->hkv, rows_dim, outer_dim, k_st, 64, box_rows, true) ||
-      !encode_map(&p.tm_v, a->v, a->dtype, a->d, a->hkv, rows_dim, outer_dim, v_st, 64, box_rows, true))
-    return FA_ERR_INVALID_ARG;
-  p.lse = lse_part;  // partials [ns][b][hkv][g] = [ns][b][hq]
-  p.o_part = o_part;
-  p.b = a->b;
-  p.sq = g;
-  p.skv = a->max_seqlen_k;
-  p.hq = a->hkv;
-  p.hkv = a->hkv;
-  p.g = 1;
-  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
-  softcap_consts(a->softcap, a->scale, &p.sc_k, &p.sc_b);
-  p.n_mtiles = static_cast<int>(ceil_div64(g, 128));
-  p.n_mcta = static_cast<int>(ceil_div64(p.n_mtiles, prefill_q_tiles(a->d)));
-  p.num_splits = ns;
-  p.blocks_per_split = 1;  // set per sequence in the kernel
-  p.max_ctas = di.sms;
-  p.status = di.status;
-  p.cu_k = paged ? nullptr : a->cu_seqlens_k;
-  p.total_k = a->num_pages;
-  p.kv_mode = paged ? kKvPaged : kKvPacked;
-  p.block_table = a->block_table;
-  p.bt_stride = a->block_table_stride;
-  p.page_size = a->page_size;
-  p.box_rows = box_rows;
-  p.seqlens = a->seqlens_k;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_prefill(p, a->d, a->dtype, st) != cudaSuccess) return FA_ERR_CUDA;
-  if (splits_used) *splits_used = ns;
-  const int64_t o_st[3] = {a->o_strides[0], a->o_strides[1], a->o_strides[1]};  // (one row: its stride is unused)
-  return fa_splitkv_combine(o_part, lse_part, ns, a->b, a->hq, 1, a->d, a->dtype, a->o, o_st, a->lse, stream);
 }
 
 fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* workspace, size_t workspace_bytes,
