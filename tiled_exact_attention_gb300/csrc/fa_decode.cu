@@ -104,7 +104,15 @@ constexpr int dec_smem_bytes() {
 }
 
 // SC: softcap, each score capped to c tanh(s / c) before the mask.
-template <int D, int G, bool BF16, bool SC>
+// Keys of sequence k of a KV cache (clamped at 0).
+__device__ __forceinline__ int cache_seq_len(const DecodeParams& p, int k) {
+  const int n = p.kv_mode == kKvPaged ? p.seqlens[k] : p.cu_seqlens[k + 1] - p.cu_seqlens[k];
+  return n > 0 ? n : 0;
+}
+
+// CACHE: a paged or packed KV cache (p.kv_mode), a separate instantiation so that
+// the dense kernel keeps its code.
+template <int D, int G, bool BF16, bool SC, bool CACHE>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecCfg<D>;
   using L = DecLane<D, G>;
@@ -117,7 +125,27 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
   int* flags = reinterpret_cast<int*>(red + kDecWarps * G * (D + 2));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, bi = blockIdx.z;
+  const int split = blockIdx.x;
+  int bi = blockIdx.z;
+  if constexpr (CACHE) {
+    // Sequences longest first: grid slice z takes the sequence of rank z by length
+    // (ties in index order), so that the hardware starts the largest CTAs first
+    // (each takes 1 / num_splits of its own sequence; measured +2.5% on 8 shuffled
+    // paged sequences of 20k-47k keys).  Small batches only.
+    if (p.b <= 64) {
+      if (threadIdx.x < p.b) {
+        const int t = threadIdx.x, lt = cache_seq_len(p, t);
+        int rank = 0;
+        for (int k = 0; k < p.b; ++k) {
+          const int lk = cache_seq_len(p, k);
+          rank += (lk > lt || (lk == lt && k < t)) ? 1 : 0;
+        }
+        if (rank == static_cast<int>(blockIdx.z)) flags[2] = t;
+      }
+      __syncthreads();
+      bi = flags[2];
+    }
+  }
   const int groups = p.g / G;                    // CTAs per KV head
   const int kvh = blockIdx.y / groups;
   const int h_first = kvh * p.g + (blockIdx.y % groups) * G;  // first query head of this CTA
@@ -495,7 +523,10 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
 template <int D, int G, bool BF16>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
-  auto kern = p.sc_b > 0.f ? fa_decode_kernel<D, G, BF16, true> : fa_decode_kernel<D, G, BF16, false>;
+  const bool sc = p.sc_b > 0.f;
+  auto kern = sc ? fa_decode_kernel<D, G, BF16, true, false> : fa_decode_kernel<D, G, BF16, false, false>;
+  if (p.kv_mode != kKvDense)
+    kern = sc ? fa_decode_kernel<D, G, BF16, true, true> : fa_decode_kernel<D, G, BF16, false, true>;
   const int smem = dec_smem_bytes<D, G>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -508,7 +539,7 @@ template <int D, int G, bool BF16>
 int dec_occupancy() {
   using C = DecCfg<D>;
   const int smem = dec_smem_bytes<D, G>();
-  auto kern = fa_decode_kernel<D, G, BF16, false>;
+  auto kern = fa_decode_kernel<D, G, BF16, false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem) != cudaSuccess || n < 1) return 1;
