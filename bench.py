@@ -15,6 +15,12 @@ reported beside it.  L2 is flushed (a 256 MiB write) before every step.
 bounded sample of the same workload.  With N > 1 (torchrun) every rank runs an
 independent replica; the line reports the total over ranks and the slowest
 rank's time.
+
+Every roofline divides by the measured burst bf16 GEMM peak (each launch lasts
+well under a millisecond, between L2 flushes); the sustained peak is reported
+beside it.  `--only NAME[,NAME...]` times just the named lines (prefill, decode,
+gqa_long, ragged_d64, ragged_d256, backward, e4m3, paged, variants, e2e, link)
+and prints them as one JSON object: the form the ncu captures use.
 """
 from __future__ import annotations
 
@@ -45,6 +51,26 @@ def _peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_tflops():
+    """(burst bf16 TFLOP/s, sustained bf16 TFLOP/s, source)."""
+    peaks, src = _peaks()
+    burst = float(peaks["bf16_tflops"])
+    return burst, float(peaks.get("bf16_tflops_sustained", burst)), src
+
+
+def _tensor_roofline(tflops, kernel=None, traffic=None, ratio=1.0, dtype_note=""):
+    """Roofline object of a tensor-core line against the burst peak (times `ratio` for another dtype)."""
+    burst, sustained, src = _peak_tflops()
+    pk = burst * ratio
+    r = {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(pk, 1), "unit": "TFLOP/s",
+         "frac": round(tflops / pk, 4), "traffic": traffic,
+         "peak_source": f"{src} bf16 burst GEMM{dtype_note} (launches of well under a millisecond)",
+         "frac_of_sustained": round(tflops / (sustained * ratio), 4)}
+    if kernel:
+        r["kernel"] = kernel
+    return r
 
 
 def _dist():
@@ -161,13 +187,11 @@ class ClockSampler:
 # ------------------------------------------------------------------------- our implementation
 
 
-def run_ours(args):
+def _setup(args):
     import torch
     import torch.distributed as dist
 
     import __graft_entry__
-    from tiled_exact_attention_gb300 import fa_fwd, fa_fwd_splitkv, fa_splitkv_default_splits, fa_sync_status
-    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -176,6 +200,65 @@ def run_ours(args):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     __graft_entry__.build()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    return ws, rank, dev, flush
+
+
+SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "backward", "e4m3", "variants", "e2e", "link")
+
+
+def run_only(args):
+    """Time only the named lines (no timed step): what the ncu captures run."""
+    import torch
+
+    names = [x for x in args.only.split(",") if x]
+    _, _, dev, flush = _setup(args)
+    steps = max(1, args.steps)
+    out = {}
+    for nm in names:
+        if nm in ("prefill", "decode"):
+            w = WORKLOADS_LAZY()[PREFILL if nm == "prefill" else DECODE]
+            out[nm] = bench_config(dev, flush, w, steps=steps, warmup=args.warmup)
+        elif nm in ("gqa_long", "ragged_d64", "ragged_d256"):
+            out[nm] = bench_config(dev, flush, WORKLOADS_LAZY()[nm], steps=steps, warmup=args.warmup)
+        elif nm == "paged":
+            out[nm] = bench_paged_decode(dev, flush, steps=steps, warmup=args.warmup)
+        elif nm == "backward":
+            out[nm] = bench_backward(dev, flush, steps=steps, warmup=args.warmup)
+        elif nm == "e4m3":
+            out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup)
+        elif nm == "variants":
+            out[nm] = bench_variants(dev, flush, steps=steps)
+        elif nm in ("e2e", "link"):
+            from tiled_exact_attention_gb300 import fa_fwd
+            from tiled_exact_attention_gb300.inputs import make_qkv
+
+            wp = WORKLOADS_LAZY()[PREFILL]
+            qc, kc, vc = make_qkv(wp)
+            stream = torch.cuda.current_stream()
+            if nm == "e2e":
+                out[nm] = {"ms_per_step": round(bench_e2e(qc, kc, vc, wp, fa_fwd, flush, stream, steps), 4)}
+            else:
+                out[nm] = bench_link(qc, kc, vc, wp, stream, steps)
+        else:
+            raise SystemExit(f"unknown line {nm!r}; one of prefill, decode, {', '.join(SECONDARY)}")
+    print(json.dumps({"only": out}), flush=True)
+
+
+def WORKLOADS_LAZY():
+    from tiled_exact_attention_gb300.inputs import WORKLOADS
+
+    return WORKLOADS
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from tiled_exact_attention_gb300 import fa_fwd, fa_fwd_splitkv, fa_splitkv_default_splits, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+
+    ws, rank, dev, flush = _setup(args)
 
     wp, wd = WORKLOADS[PREFILL], WORKLOADS[DECODE]
     qc, kc, vc = make_qkv(wp)
@@ -191,7 +274,6 @@ def run_ours(args):
 
     wsb = fa_splitkv_workspace_size(dq, dk, dv, ns, causal=True, q_pos_offset=wd.offset)
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def prefill():
         fa_fwd(q, k, v, causal=True, q_pos_offset=wp.offset, out=o, lse=lse)
@@ -237,15 +319,20 @@ def run_ours(args):
     pre_avg = sum(pre_ms) / K
     dec_avg = sum(dec_ms) / K
     step_ms = pre_avg + dec_avg
+    del q, k, v, o, dq, dk, dv, do, work
 
-    # ---- end-to-end through the public call with host buffers (prefill) ----
-    e2e_ms = bench_e2e(qc, kc, vc, wp, fa_fwd, flush, stream, max(3, min(50, K // 20)), dist if ws > 1 else None)
+    # ---- end-to-end through the public call with host buffers (prefill), and the link alone ----
+    e2e_steps = max(3, min(50, K // 20))
+    e2e_ms = bench_e2e(qc, kc, vc, wp, fa_fwd, flush, stream, e2e_steps, dist if ws > 1 else None)
+    link = bench_link(qc, kc, vc, wp, stream, e2e_steps)
 
+    few = max(10, min(100, K // 50))
+    configs = {nm: bench_config(dev, flush, WORKLOADS[nm], steps=few) for nm in ("gqa_long", "ragged_d64",
+                                                                                 "ragged_d256")}
     paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
-    bwd = bench_backward(dev, flush, steps=max(10, min(100, K // 50)))
+    bwd = bench_backward(dev, flush, steps=few)
     e4m3 = bench_e4m3(dev, flush, steps=max(10, min(200, K // 25)))
-    variants = bench_variants(dev, flush, float(_peaks()[0].get("bf16_tflops_sustained", _peaks()[0]["bf16_tflops"])),
-                              steps=max(10, min(100, K // 50)))
+    variants = bench_variants(dev, flush, steps=few)
 
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
     kv_bytes = 2 * wd.b * wd.hkv * wd.skv * wd.d * 2
@@ -263,13 +350,18 @@ def run_ours(args):
     tflops = job_throughput(flops, ws, pre_avg) / 1e12
     per_gpu_tflops = flops / (pre_avg * 1e-3) / 1e12
     dec_gbs = dec_bytes / (dec_avg * 1e-3) / 1e9
-    pk = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    pk_burst = float(peaks["bf16_tflops"])
     hbm = float(peaks["hbm_gbs"])
     h2d = sum(t.numel() * t.element_size() for t in (qc, kc, vc))
-    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    d2h = wp.b * wp.sq * wp.hq * wp.d * 2 + wp.b * wp.hq * wp.sq * 4
     pre_traffic = _profiled_traffic("fa_prefill_kernel")
     dec_traffic = _profiled_traffic("fa_decode_kernel")
+    e4 = dict(e4m3)
+    e4["roofline"] = _tensor_roofline(e4m3["value"], kernel=e4m3["kernel"],
+                                      traffic=_profiled_traffic("fa_prefill_kernel_e4m3"), ratio=2.0,
+                                      dtype_note=" x 2 (the nominal fp8 : bf16 ratio)")
+    bw = dict(bwd)
+    bw["roofline"] = _tensor_roofline(bwd["value"], kernel="fa_bwd_dkdv_kernel (the larger of the two product kernels)",
+                                      traffic=_profiled_traffic("fa_bwd_dkdv_kernel"))
     line = {
         "metric": METRIC,
         "value": round(tflops, 2),
@@ -299,34 +391,31 @@ def run_ours(args):
             "unit": "GB/s",
             "ms_per_step": round(dec_avg, 4),
             "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(dec_gbs / hbm, 4), "peak_source": peak_src,
+                         "frac": round(dec_gbs / hbm, 4), "peak_source": f"{peak_src} copy bandwidth",
                          "traffic": dec_traffic, "spec_peak": 8000.0,
                          "frac_of_spec": round(dec_gbs / 8000.0, 4),
                          "note": "phase time = split kernel with the fused merge (+ a memset of its counters)"},
         },
+        "gqa_long": configs["gqa_long"],
+        "ragged_d64": configs["ragged_d64"],
+        "ragged_d256": configs["ragged_d256"],
         "decode_paged": dict(paged, roofline={"bound": "hbm", "achieved": paged["value"], "peak": hbm,
                                               "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
-                                              "peak_source": peak_src, "traffic": None}),
-        "e4m3": dict(e4m3, roofline={"bound": "tensor", "achieved": e4m3["value"],
-                                     "peak": round(2 * pk, 1), "unit": "TFLOP/s", "frac": round(e4m3["value"] / (2 * pk), 4),
-                                     "peak_source": f"{peak_src} bf16 sustained x 2 (the nominal fp8 : bf16 ratio)",
-                                     "traffic": _profiled_traffic("fa_prefill_kernel_e4m3")}),
-        "backward": dict(bwd, roofline={"bound": "tensor", "achieved": bwd["value"], "peak": pk, "unit": "TFLOP/s",
-                                        "frac": round(bwd["value"] / pk, 4), "peak_source": f"{peak_src} sustained",
-                                        "frac_of_burst": round(bwd["value"] / pk_burst, 4),
-                                        "traffic": _profiled_traffic("fa_bwd_dkdv_kernel"),
-                                        "traffic_kernel": "fa_bwd_dkdv_kernel (the larger of the two product kernels)"}),
+                                              "peak_source": f"{peak_src} copy bandwidth", "traffic": None}),
+        "e4m3": e4,
+        "backward": bw,
         "variants": variants,
-        "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2), "peak": pk, "unit": "TFLOP/s",
-                     "frac": round(per_gpu_tflops / pk, 4), "traffic": pre_traffic,
-                     "kernel": "fa_prefill_kernel<128, bf16>",
-                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
-                     "frac_of_burst": round(per_gpu_tflops / pk_burst, 4), "spec_peak": 2250.0,
-                     "frac_of_spec": round(per_gpu_tflops / 2250.0, 4)},
+        "roofline": dict(_tensor_roofline(per_gpu_tflops, kernel="fa_prefill_kernel<128, bf16>", traffic=pre_traffic),
+                         spec_peak=2250.0, frac_of_spec=round(per_gpu_tflops / 2250.0, 4)),
         "clocks": clocks,
         "e2e": {"value": round(job_throughput(flops, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step; pipelined over two buffer sets (step i + 1 copies in while step i computes and copies out)"},
+                "copy_only_ms": link["ms_per_step"],
+                "frac_of_copy_bound": round(link["ms_per_step"] / e2e_ms, 4),
+                "link": link,
+                "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step; "
+                        "pipelined over two buffer sets (step i + 1 copies in while step i computes and copies out); "
+                        "copy_only_ms = the same copies with no computation (the link's own time per step)"},
         "gpu_launches": K * 2,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -335,6 +424,96 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def bench_config(dev, flush, w, steps=30, warmup=3):
+    """One forward workload of the target set (the long causal GQA prefill, the ragged-tail d = 64 / 256
+    forward passes; also the timed step's prefill and decode when asked alone), in TFLOP/s of the visible
+    (query, key) pairs (4 d flops per pair and head) or, for the split-KV decode, KV GB/s."""
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_fwd, fa_fwd_splitkv, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import make_qkv
+
+    q, k, v = (t.to(dev) for t in make_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.b, w.hq, w.sq), dtype=torch.float32, device=dev)
+    off = w.offset if w.causal else None
+    if w.sq == 1:
+        ms = _timed(lambda: fa_fwd_splitkv(q, k, v, causal=True, q_pos_offset=w.offset, out=o, lse=lse), flush,
+                    steps, warmup)
+        nbytes = 2 * w.b * w.hkv * w.skv * w.d * 2 + 2 * (w.b * w.hq * w.d * 2) + w.b * w.hq * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        hbm = float(_peaks()[0]["hbm_gbs"])
+        return {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4), "bytes_per_launch": nbytes,
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(gbs / hbm, 4), "traffic": _profiled_traffic("fa_decode_kernel")}}
+    ms = _timed(lambda: fa_fwd(q, k, v, causal=w.causal, q_pos_offset=off, out=o, lse=lse), flush, steps, warmup)
+    if fa_sync_status() != 0:
+        raise RuntimeError(f"device status set by the {w.name} forward pass")
+    flops = 4.0 * w.d * w.visible_pairs_per_head() * w.b * w.hq
+    tf = flops / (ms * 1e-3) / 1e12
+    dt = "bf16" if w.dtype == "bf16" else "fp16"
+    kname = "fa_prefill_kernel" if w.d == 128 else f"fa_prefill_kernel_d{w.d}"
+    return {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "flops_per_launch": flops,
+            "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "dtype": dt,
+                       "std": w.std, "causal": w.causal},
+            "roofline": _tensor_roofline(tf, kernel=f"fa_prefill_kernel<{w.d}, {dt}>",
+                                         traffic=_profiled_traffic(kname) if w.d != 128 else None,
+                                         dtype_note=" (fp16 runs at the bf16 rate)" if dt == "fp16" else ""),
+            "steps": steps}
+
+
+def bench_link(qc, kc, vc, wp, stream, steps):
+    """The host link alone: the end-to-end step's copies (pinned Q, K, V in on three streams, O and LSE out on a
+    fourth), the same bytes and overlap, with no computation; plus each direction by itself."""
+    import torch
+
+    dev = stream.device
+    h_in = [t.pin_memory() for t in (qc, kc, vc)]
+    d_in = [torch.empty_like(t, device=dev) for t in (qc, kc, vc)]
+    o = torch.empty(qc.shape, dtype=qc.dtype, device=dev)
+    lse = torch.empty((wp.b, wp.hq, wp.sq), dtype=torch.float32, device=dev)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    s_out = torch.cuda.Stream(device=dev)
+
+    def both(n, do_in=True, do_out=True):
+        for si in s_in + [s_out]:
+            si.wait_stream(stream)
+        for _ in range(n):
+            if do_in:
+                for j in range(3):
+                    with torch.cuda.stream(s_in[j]):
+                        d_in[j].copy_(h_in[j], non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    ho.copy_(o, non_blocking=True)
+                    hl.copy_(lse, non_blocking=True)
+        for si in s_in + [s_out]:
+            stream.wait_stream(si)
+
+    def timed(**kw):
+        both(2, **kw)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        both(steps, **kw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    h2d = sum(t.numel() * t.element_size() for t in (qc, kc, vc))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    ms = timed()
+    ms_in = timed(do_out=False)
+    ms_out = timed(do_in=False)
+    return {"ms_per_step": round(ms, 4), "h2d_gbs": round(h2d / (ms_in * 1e-3) / 1e9, 1),
+            "d2h_gbs": round(d2h / (ms_out * 1e-3) / 1e9, 1),
+            "both_gbs": round((h2d + d2h) / (ms * 1e-3) / 1e9, 1),
+            "what": "cudaMemcpyAsync from / to pinned host buffers (torch copy_), three copy-in streams and one "
+                    "copy-out stream side by side"}
 
 
 def bench_backward(dev, flush, steps=30, warmup=3):
@@ -438,14 +617,15 @@ def _timed(step, flush, steps, warmup=3):
     return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
 
 
-def bench_variants(dev, flush, pk, steps=20):
+def bench_variants(dev, flush, steps=20):
     """The mask and layout variants of the forward pass, each on a prefill-sized problem, in TFLOP/s of the
     visible (query, key) pairs (4 d flops per pair and head), against the sustained bf16 peak:
       * window: the causal prefill workload with a sliding window of 1024 keys (local causal);
       * softcap: the causal prefill workload with every score capped to 30 tanh(s / 30);
       * varlen: 16 packed causal sequences, lengths drawn (seeded) from [256, 4096], H = 16, d = 128;
       * decode_g8: split-KV decode with 8 query heads per KV head (B = 8, Hq = 64, Hkv = 8, KV = 32768,
-        d = 128), whose heads are the rows of one tensor-core tile; KV GB/s against the measured copy peak."""
+        d = 128), whose heads are the rows of one tensor-core tile; KV GB/s against the measured copy peak.
+    The tensor-core lines divide by the burst bf16 peak."""
     import numpy as np
     import torch
 
@@ -464,15 +644,13 @@ def bench_variants(dev, flush, pk, steps=20):
     tf = 4.0 * w.d * pairs * w.b * w.hq / (ms * 1e-3) / 1e12
     out["window"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
                      "config": {"b": w.b, "sq": w.sq, "hq": w.hq, "d": w.d, "causal": True, "window": [wl, 0]},
-                     "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
-                                  "frac": round(tf / pk, 4), "traffic": None}}
+                     "roofline": _tensor_roofline(tf)}
     pairs = w.visible_pairs_per_head()
     ms = _timed(lambda: fa_fwd(q, k, v, causal=True, softcap=30.0, out=o, lse=lse), flush, steps)
     tf = 4.0 * w.d * pairs * w.b * w.hq / (ms * 1e-3) / 1e12
     out["softcap"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
                       "config": {"b": w.b, "sq": w.sq, "hq": w.hq, "d": w.d, "causal": True, "softcap": 30.0},
-                      "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
-                                   "frac": round(tf / pk, 4), "traffic": None}}
+                      "roofline": _tensor_roofline(tf)}
     rng = np.random.default_rng(BASE_SEED + 60)
     lens = rng.integers(256, 4097, size=16).astype(np.int64)
     total = int(lens.sum())
@@ -491,8 +669,7 @@ def bench_variants(dev, flush, pk, steps=20):
     out["varlen"] = {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
                      "config": {"sequences": len(lens), "lengths": [int(x) for x in lens], "hq": hq, "d": d,
                                 "causal": True},
-                     "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk, "unit": "TFLOP/s",
-                                  "frac": round(tf / pk, 4), "traffic": None}}
+                     "roofline": _tensor_roofline(tf)}
     from tiled_exact_attention_gb300 import fa_fwd_splitkv
     from tiled_exact_attention_gb300.api import fa_splitkv_workspace_size
     from tiled_exact_attention_gb300.inputs import make_custom
@@ -756,11 +933,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--only", default="", help="time only these lines (comma-separated); prints them alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 

@@ -235,7 +235,12 @@ size_t fa_kvcache_workspace_size(const fa_kvcache_args* args, int32_t num_splits
  * whatever the cache holds there never reaches O); otherwise the CUDA-core
  * kernel merges the splits itself.  The workspace is caller-owned device memory
  * of at least fa_kvcache_workspace_size bytes, 256-byte aligned, under the same
- * rules as fa_fwd_splitkv's.
+ * rules as fa_fwd_splitkv's.  The lengths live on the device, so the kernels
+ * check them before reading anything they address: a paged sequence longer
+ * than block_table_stride * page_size keys, or a packed sequence whose
+ * [cu_seqlens_k[b], cu_seqlens_k[b + 1]) is not inside [0, num_pages), is not
+ * read at all; FA_ERR_DEVICE_ARG is recorded for the next fa_sync_status and
+ * that sequence's O and LSE are undefined (the other sequences are computed).
  */
 fa_status fa_fwd_kvcache(const fa_kvcache_args* args, int32_t num_splits, void* workspace, size_t workspace_bytes,
                          int32_t* splits_used, void* stream);

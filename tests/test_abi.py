@@ -154,10 +154,14 @@ def test_validation_strides_and_null(lib):
     a = _args(sq=0)
     assert lib.fa_fwd(ctypes.byref(a), None) == 0  # nothing to do
     assert lib.fa_splitkv_workspace_size(None, 1) == 0
-    a = _args()
+    a = _args(skv=1024)  # 8 key blocks
     ws = lib.fa_splitkv_workspace_size(ctypes.byref(a), 3)
     rows = 3 * 1 * 2 * 128
     assert ws >= rows * 128 * 4 + rows * 4
+    # a request above the key blocks there are is sized as the split count the call will
+    # use (capped at the blocks): 128 keys are one block, so 3 splits size as 1
+    a = _args()
+    assert lib.fa_splitkv_workspace_size(ctypes.byref(a), 3) == lib.fa_splitkv_workspace_size(ctypes.byref(a), 1)
     assert lib.fa_fwd_splitkv(ctypes.byref(a), -1, None, 0, None, None) == 1
 
 

@@ -96,3 +96,49 @@ def test_backward_no_query_rows_gives_zero_key_gradients():
     dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=True, q_pos_offset=-10, dk=dk, dv=dv)
     assert fa_sync_status() == 0
     assert torch.all(dq == 0) and torch.all(dk == 0) and torch.all(dv == 0)
+
+
+FULL = [
+    # b, sq, hq, hkv (d = 128, bf16, causal)
+    (1, 4096, 4, 4),
+    (1, 2048, 32, 8),   # the long GQA workload's head ratio: 32 query heads over 8 KV heads
+]
+
+
+@pytest.mark.parametrize("case", FULL, ids=lambda c: "-".join(str(x) for x in c))
+def test_backward_long_sequences(case):
+    """Causal backward on thousands of rows, every gradient entry against the oracle."""
+    b, s, hq, hkv = case
+    d, dt = 128, torch.bfloat16
+    seed = _seed(case)
+    q, k, v = (t.to(DEV) for t in make_custom(b, s, s, hq, hkv, d, "bf16", std=1.0, seed=seed))
+    do = normal((b, s, hq, d), seed, 7, 1.0, dt).to(DEV)
+    o, lse = fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = fa_bwd(q, k, v, o, lse, do, causal=True)
+    assert fa_sync_status() == 0
+    rq, rk, rv = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), causal=True, scale=1.0 / math.sqrt(d))
+    what = str(case)
+    _check("dQ", dq, rq, dt, what)
+    _check("dK", dk, rk, dt, what)
+    _check("dV", dv, rv, dt, what)
+
+
+def test_backward_benchmark_workload():
+    """The backward benchmark's own inputs and launch (B=4, H=16, N=4096, d=128,
+    causal, upstream gradient from the same seeded stream), every entry against
+    the oracle."""
+    from tiled_exact_attention_gb300.inputs import BASE_SEED, WORKLOADS, make_qkv
+
+    w = WORKLOADS["causal_prefill"]
+    q, k, v = (t.to(DEV) for t in make_qkv(w))
+    do = normal(tuple(q.shape), BASE_SEED + w.index, 7, 1.0, q.dtype).to(DEV)
+    o, lse = fa_fwd(q, k, v, causal=True, q_pos_offset=w.offset)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=DEV)
+    fa_bwd(q, k, v, o, lse, do, causal=True, q_pos_offset=w.offset, dq=dq, dk=dk, dv=dv, workspace=ws)
+    assert fa_sync_status() == 0
+    rq, rk, rv = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), causal=True, q_pos_offset=w.offset,
+                                      scale=1.0 / math.sqrt(w.d))
+    _check("dQ", dq, rq, q.dtype, "benchmark workload")
+    _check("dK", dk, rk, q.dtype, "benchmark workload")
+    _check("dV", dv, rv, q.dtype, "benchmark workload")

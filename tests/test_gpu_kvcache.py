@@ -163,3 +163,67 @@ def test_paged_matches_contiguous_decode():
     assert (o.float() - o_ref[:, 0].float()).abs().max().item() <= 2e-2
     assert (lse - l_ref[:, :, 0]).abs().max().item() <= 1e-3
 
+
+
+@pytest.mark.parametrize("hq,ns", [(8, 1), (8, 3), (16, 1), (16, 3)])
+def test_paged_length_past_its_table_row_is_rejected_on_the_device(hq, ns):
+    """A sequence length that needs more pages than its block-table row holds is
+    caught by the kernels before any table read: the sequence is skipped,
+    FA_ERR_DEVICE_ARG is reported, the other sequences are still computed.  (The
+    table is a view into a taller allocation, so even an unchecked read past the
+    row would stay inside memory the test owns.)"""
+    from tiled_exact_attention_gb300._lib import FA_ERR_DEVICE_ARG
+
+    b, hkv, d, ps, dt = 3, 2, 128, 128, torch.bfloat16
+    lens = [700, 300, 500]
+    width = 6  # pages per table row: 768 keys at most
+    seed = 515 + hq
+    q = normal((b, hq, d), seed, 1, 1.0, dt)
+    ks, vs = _sequences(lens, hkv, d, dt, seed)
+    num_pages = b * width + 8
+    k_pool = torch.zeros((num_pages, ps, hkv, d), dtype=dt)
+    v_pool = torch.zeros((num_pages, ps, hkv, d), dtype=dt)
+    table_alloc = np.zeros((b + 4, width), dtype=np.int32)
+    for i, n in enumerate(lens):
+        for pg in range(math.ceil(n / ps)):
+            page = i * width + pg
+            table_alloc[i, pg] = page
+            lo, hi = pg * ps, min(n, (pg + 1) * ps)
+            k_pool[page, : hi - lo] = ks[i][lo:hi]
+            v_pool[page, : hi - lo] = vs[i][lo:hi]
+    table = torch.from_numpy(table_alloc).to(DEV)[:b]
+    seqlens = torch.tensor([lens[0], width * ps + 1, lens[2]], dtype=torch.int32, device=DEV)
+    assert fa_sync_status() == 0
+    o, lse = fa_fwd_kvcache(q.to(DEV), k_pool.to(DEV), v_pool.to(DEV), block_table=table, seqlens_k=seqlens,
+                            max_seqlen_k=max(lens), num_splits=ns)
+    assert fa_sync_status() == FA_ERR_DEVICE_ARG
+    assert fa_sync_status() == 0  # reported once, then cleared
+    o_ref, l_ref = _oracle(q, ks, vs)
+    keep = [0, 2]
+    _check(o[keep], lse[keep], o_ref[keep], l_ref[keep], dt, f"paged, bad length, hq={hq} ns={ns}")
+
+
+@pytest.mark.parametrize("hq", [8, 16])
+def test_packed_offsets_past_the_rows_are_rejected_on_the_device(hq):
+    """Packed keys whose prefix sums run past the declared rows: the sequence is
+    skipped and FA_ERR_DEVICE_ARG reported; the others are still computed.  (The
+    declared rows are a view of a longer tensor.)"""
+    from tiled_exact_attention_gb300._lib import FA_ERR_DEVICE_ARG
+
+    hkv, d, dt = 2, 128, torch.bfloat16
+    lens = [400, 300, 1000]
+    seed = 616 + hq
+    q = normal((3, hq, d), seed, 1, 1.0, dt)
+    ks, vs = _sequences(lens, hkv, d, dt, seed)
+    k = torch.cat(ks).to(DEV)
+    v = torch.cat(vs).to(DEV)
+    declared = lens[0] + lens[1] + 200  # the last sequence runs 800 rows past the declared end
+    cu = torch.tensor([0, lens[0], lens[0] + lens[1], sum(lens)], dtype=torch.int32, device=DEV)
+    assert fa_sync_status() == 0
+    o, lse = fa_fwd_kvcache(q.to(DEV), k[:declared], v[:declared], cu_seqlens_k=cu, max_seqlen_k=max(lens),
+                            num_splits=2)
+    assert fa_sync_status() == FA_ERR_DEVICE_ARG
+    assert fa_sync_status() == 0
+    o_ref, l_ref = _oracle(q, ks, vs)
+    keep = [0, 1]
+    _check(o[keep], lse[keep], o_ref[keep], l_ref[keep], dt, f"packed, bad offsets, hq={hq}")

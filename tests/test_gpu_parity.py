@@ -95,19 +95,45 @@ def test_ragged_n5_tile_case():
     _full_compare(q, k, v, True, w.offset, 1.0 / math.sqrt(w.d), o, lse, "ragged_n5")
 
 
-@pytest.mark.parametrize("name", ["causal_prefill", "gqa_long", "ragged_d64", "ragged_d256"])
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["causal_prefill", "ragged_d64", "ragged_d256"])
+def test_full_size_every_row(name):
+    """Every row of the causal-prefill and ragged-tail workloads at their full size,
+    in the launch configuration the benchmark times (persistent grid, default
+    tiles), against the oracle: a tile-schedule mistake that touches only a few
+    (batch, head, row-block) items of the persistent scheduler cannot hide."""
     w = WORKLOADS[name]
     qc, kc, vc = make_qkv(w)
     q, k, v = _cuda(qc, kc, vc)
     o, lse = fa_fwd(q, k, v, causal=w.causal, q_pos_offset=w.offset if w.causal else None)
     assert fa_sync_status() == 0
-    rows = sample_rows(w.b, w.hq, w.sq, n_random=64, seed=w.index)
+    rows = oracle.all_rows(w.b, w.hq, w.sq)
     o_ref, l_ref = oracle_rows(qc, kc, vc, causal=w.causal, q_pos_offset=w.offset, scale=1.0 / math.sqrt(w.d),
                                rows=rows)
     og, lg = gather(o, lse, rows)
     assert_parity(og, lg, o_ref, l_ref, qc.dtype, name)
-    # property that holds for every row: all outputs finite, LSE finite where a key is visible
+
+
+def test_gqa_long_whole_heads():
+    """The long GQA workload (B=1, Hq=32, Hkv=8, N=16384): four whole query heads
+    (two sharing KV head 0, one in the middle, the last), the first 256 rows of
+    every head (the row groups the longest-first schedule runs last), and a
+    random sample over all heads."""
+    w = WORKLOADS["gqa_long"]
+    qc, kc, vc = make_qkv(w)
+    q, k, v = _cuda(qc, kc, vc)
+    o, lse = fa_fwd(q, k, v, causal=True, q_pos_offset=w.offset)
+    assert fa_sync_status() == 0
+    rows = {tuple(r) for r in sample_rows(w.b, w.hq, w.sq, n_random=256, seed=w.index)}
+    for h in (0, 1, 13, w.hq - 1):
+        rows.update((0, h, i) for i in range(w.sq))
+    for h in range(w.hq):
+        rows.update((0, h, i) for i in range(256))
+    rows = np.array(sorted(rows), dtype=np.int64)
+    o_ref, l_ref = oracle_rows(qc, kc, vc, causal=True, q_pos_offset=w.offset, scale=1.0 / math.sqrt(w.d),
+                               rows=rows)
+    og, lg = gather(o, lse, rows)
+    assert_parity(og, lg, o_ref, l_ref, qc.dtype, "gqa_long")
+    # a property that holds for every row: every row sees at least its own key
     assert torch.isfinite(o).all()
     assert torch.isfinite(lse).all()
 

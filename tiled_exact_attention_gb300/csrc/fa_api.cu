@@ -238,24 +238,30 @@ struct SplitShape {
   int64_t nblk;
 };
 
+// Key blocks a split range is cut from, per path (host-only: no device query).
+int64_t split_blocks(const fa_fwd_args* a) {
+  if (use_head_rows(a)) return ceil_div64(decode_kv_limit(a), prefill_block_n(a->d));
+  if (use_decode_kernel(a))
+    return ceil_div64(decode_kv_limit(a), decode_block_n(a->d)) - decode_kv_start(a) / decode_block_n(a->d);
+  return ceil_div64(a->skv, prefill_block_n(a->d));
+}
+
 bool split_shape(const fa_fwd_args* a, const DeviceInfo& di, SplitShape* s) {
+  s->nblk = split_blocks(a);
   if (use_head_rows(a)) {
     const int g = a->hq / a->hkv;
     const int64_t n_mcta = ceil_div64(ceil_div64(g, 128), prefill_q_tiles(a->d));
     s->units = static_cast<int64_t>(a->b) * a->hkv * n_mcta;
     s->slots = di.sms;
-    s->nblk = ceil_div64(decode_kv_limit(a), prefill_block_n(a->d));
   } else if (use_decode_kernel(a)) {
     const int g = a->hq / a->hkv;
     s->units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
     s->slots = static_cast<int64_t>(di.sms) * decode_ctas_per_sm(a->d, a->dtype);
-    s->nblk = ceil_div64(decode_kv_limit(a), decode_block_n(a->d)) - decode_kv_start(a) / decode_block_n(a->d);
   } else {
     const int nq = prefill_q_tiles(a->d);
     const int64_t n_mcta = ceil_div64(ceil_div64(a->sq, 128), nq);
     s->units = static_cast<int64_t>(a->b) * a->hq * n_mcta;
     s->slots = di.sms;
-    s->nblk = ceil_div64(a->skv, prefill_block_n(a->d));
   }
   return true;
 }
@@ -387,15 +393,21 @@ int kvcache_splits(const fa_kvcache_args* a, int32_t requested, const DeviceInfo
   return ns < 1 ? 1 : ns;
 }
 
+// A split count capped at the key blocks there are (a split with no block is
+// useless) and at kMaxSplits * 8.
+int cap_splits(const fa_fwd_args* a, int64_t ns) {
+  const int64_t nblk = split_blocks(a);
+  const int64_t cap = nblk > 0 ? nblk : 1;
+  if (ns > cap) ns = cap;
+  if (ns > kMaxSplits * 8) ns = kMaxSplits * 8;
+  return ns < 1 ? 1 : static_cast<int>(ns);
+}
+
 int resolve_splits(const fa_fwd_args* a, int32_t requested, const DeviceInfo& di) {
+  if (requested > 0) return cap_splits(a, requested);
   SplitShape s{};
   split_shape(a, di, &s);
-  int ns = requested > 0 ? requested
-                         : fa_num_splits_heuristic(s.units, s.slots, s.nblk, kMaxSplits);
-  const int64_t cap = s.nblk > 0 ? s.nblk : 1;
-  if (ns > cap) ns = static_cast<int>(cap);
-  if (ns > kMaxSplits * 8) ns = kMaxSplits * 8;
-  return ns < 1 ? 1 : ns;
+  return cap_splits(a, fa_num_splits_heuristic(s.units, s.slots, s.nblk, kMaxSplits));
 }
 
 }  // namespace
@@ -542,13 +554,12 @@ int32_t fa_splitkv_default_splits(const fa_fwd_args* a) {
 
 size_t fa_splitkv_workspace_size(const fa_fwd_args* a, int32_t num_splits) {
   if (validate(a) != FA_OK || num_splits < 0) return 0;
-  int ns = num_splits;
-  if (ns == 0) {
-    DeviceInfo di;
-    if (!device_info(&di)) return 0;
-    ns = resolve_splits(a, 0, di);
-  }
-  return workspace_bytes_for(a, ns);
+  // the split count fa_fwd_splitkv will use: a request capped at the key blocks
+  // there are (no device needed), or the heuristic's
+  if (num_splits > 0) return workspace_bytes_for(a, cap_splits(a, num_splits));
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  return workspace_bytes_for(a, resolve_splits(a, 0, di));
 }
 
 fa_status fa_splitkv_combine(const float* o_part, const float* lse_part, int32_t num_splits, int32_t b, int32_t hq,
@@ -804,6 +815,7 @@ fa_status fa_fwd_kvcache(const fa_kvcache_args* a, int32_t num_splits, void* wor
   p.box_rows = box_rows;
   p.seqlens = a->seqlens_k;
   p.cu_seqlens = a->cu_seqlens_k;
+  p.total_k = a->num_pages;
   p.counters = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(lse_part) + align256(rows * sizeof(float)));
   p.o = a->o;
   p.o_stride_b = a->o_strides[0];

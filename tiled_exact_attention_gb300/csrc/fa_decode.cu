@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -153,11 +155,24 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
   // (contiguous, paged or packed).
   int limit = p.kv_limit, start = p.kv_start, nblk = p.nblk, bps = p.blocks_per_split, row_base = 0;
   if (p.kv_mode != kKvDense) {
+    // The lengths live on the device, so they are checked here before anything
+    // they address is read: a paged sequence may not outrun its block-table row,
+    // a packed one must lie inside the packed rows.  A sequence that fails is not
+    // read (its keys count as none) and FA_ERR_DEVICE_ARG is recorded.
+    bool seq_ok;
     if (p.kv_mode == kKvPaged) {
       limit = p.seqlens[bi];
+      seq_ok = static_cast<int64_t>(limit) <= p.bt_stride * p.page_size;
     } else {
       row_base = p.cu_seqlens[bi];
-      limit = p.cu_seqlens[bi + 1] - row_base;
+      const int end = p.cu_seqlens[bi + 1];
+      seq_ok = row_base >= 0 && end >= row_base && end <= p.total_k;
+      limit = end - row_base;
+    }
+    if (!seq_ok) {
+      if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) record_error(p.status, kErrDeviceArg);
+      limit = 0;
+      row_base = 0;
     }
     limit = max(limit, 0);
     start = p.window_left >= 0 ? max(0, limit - 1 - p.window_left) : 0;
@@ -640,14 +655,28 @@ int decode_heads_per_cta(int g) { return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1
 
 bool decode_supported(int d, int g) { return (d == 64 || d == 128 || d == 256) && g >= 1; }
 
+// Resident decode CTAs per SM, from the occupancy query on the first call per
+// (device, d, dtype) and cached: the split heuristic asks on every split-KV call.
 int decode_ctas_per_sm(int d, int dtype) {
+  constexpr int kDevs = 64;
+  static std::atomic<int> cache[kDevs][3][2];  // 0 = not yet queried (static storage starts zeroed)
   const bool bf16 = dtype == 0;
-  switch (d) {
-    case 64: return bf16 ? dec_occupancy<64, 4, true>() : dec_occupancy<64, 4, false>();
-    case 128: return bf16 ? dec_occupancy<128, 4, true>() : dec_occupancy<128, 4, false>();
-    case 256: return bf16 ? dec_occupancy<256, 4, true>() : dec_occupancy<256, 4, false>();
-    default: return 1;
+  const int di = d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : -1;
+  if (di < 0) return 1;
+  int dev = -1;
+  const bool cacheable = cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kDevs;
+  if (cacheable) {
+    const int n = cache[dev][di][bf16 ? 1 : 0].load(std::memory_order_relaxed);
+    if (n > 0) return n;
   }
+  int n = 1;
+  switch (d) {
+    case 64: n = bf16 ? dec_occupancy<64, 4, true>() : dec_occupancy<64, 4, false>(); break;
+    case 128: n = bf16 ? dec_occupancy<128, 4, true>() : dec_occupancy<128, 4, false>(); break;
+    default: n = bf16 ? dec_occupancy<256, 4, true>() : dec_occupancy<256, 4, false>(); break;
+  }
+  if (cacheable) cache[dev][di][bf16 ? 1 : 0].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int dtype, cudaStream_t stream) {

@@ -89,6 +89,7 @@ struct DecodeParams {
   int box_rows;                 // rows per TMA box: the key block, or 64 when pages are smaller than it
   const int* seqlens;           // paged: [b] keys per sequence
   const int* cu_seqlens;        // packed: [b + 1] prefix sums of keys per sequence
+  int total_k;                  // packed: rows of the packed K / V
   // Fused merge: the last split of a (batch, query-head group) to finish merges
   // all splits' partials into o / lse.  counters: one int per (batch, group),
   // zero at launch; the merging CTA puts its counter back to zero.

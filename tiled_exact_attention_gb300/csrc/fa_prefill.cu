@@ -125,12 +125,20 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
   if constexpr (CACHE) {
     // KV cache: dense Q; the sequence's own keys, paged or packed (clamped
     // lengths; a page or row outside the cache reads as zeros, never faults)
+    // The lengths live on the device and are checked before anything they
+    // address is read: a paged sequence may not outrun its block-table row, a
+    // packed one must lie inside the packed rows (else the item is skipped and
+    // FA_ERR_DEVICE_ARG recorded).
     w.tbk = 0;
     if (p.kv_mode == kKvPaged) {
-      w.skv = max(p.seqlens[w.bi], 0);
+      const int len = p.seqlens[w.bi];
+      w.valid = static_cast<int64_t>(len) <= static_cast<int64_t>(p.bt_stride) * p.page_size;
+      w.skv = w.valid ? max(len, 0) : 0;
     } else {
-      w.k_base = p.cu_k[w.bi];
-      w.skv = max(p.cu_k[w.bi + 1] - w.k_base, 0);
+      const int beg = p.cu_k[w.bi], end = p.cu_k[w.bi + 1];
+      w.valid = beg >= 0 && end >= beg && end <= p.total_k;
+      w.k_base = w.valid ? beg : 0;
+      w.skv = w.valid ? end - beg : 0;
     }
   } else if constexpr (VARLEN) {
     // Packed: sequence bi owns Q rows [cu_q[bi], cu_q[bi + 1]) and K/V rows
