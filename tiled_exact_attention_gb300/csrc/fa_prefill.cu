@@ -673,8 +673,8 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
           }
         }
         // P = 2^(s * scale * log2 e - m), written over the first half of the S
-        // columns as packed 16-bit pairs; the MMA warp is signalled once per block
-        // (a second, earlier signal for half of P measured slower).
+        // columns as packed 16-bit pairs; the MMA warp is signalled once per block,
+        // or once per half of the block's keys (HALF_P).
         const float2 sl2v = SC ? make_float2(1.f, 1.f) : make_float2(sl2b, sl2b);
         const float2 negm = make_float2(-m_use, -m_use);
         float2 sum2[4];
@@ -709,8 +709,17 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             const int cc = half * (BN / 2) + c;
             const float2 x = __ffma2_rn(make_float2(s[cc], s[cc + 1]), sl2v, negm);
             const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
             pk[c >> 1] = pack2<BF16>(e.x, e.y);
+            if constexpr (BF16) {
+              sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
+            } else {
+              // fp16: l sums P as rounded for the P V product, so that O = o / l
+              // weighs every key by exactly the factor its V row was multiplied
+              // with (a dominant key's 2^-11 rounding would otherwise reach O in
+              // full); LSE keeps that rounding, well inside its bound.  bf16 sums
+              // the unrounded P: its 2^-9 rounding would reach LSE.
+              add_packed_f16(sum2[(c >> 1) & 3], pk[c >> 1]);
+            }
           }
 #pragma unroll
           for (int c = 0; c < BN / 4; c += 16)

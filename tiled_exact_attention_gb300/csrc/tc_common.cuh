@@ -89,6 +89,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// a.x += lo, a.y += hi for a packed pair of fp16 values, each widened exactly to
+// fp32 (mixed-precision add).
+__device__ __forceinline__ void add_packed_f16(float2& a, uint32_t u) {
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(a.x), "+f"(a.y)
+      : "r"(u));
+}
+
 // S_t = Q_t K^T over the head dimension: D / 16 MMAs of K = 16, both operands
 // K-major with 128-byte swizzle (64-column chunks of 128-byte rows).
 template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool W = false>
