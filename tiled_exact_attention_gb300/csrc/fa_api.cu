@@ -1012,6 +1012,16 @@ fa_status fa_bwd(const fa_bwd_args* a, void* workspace, size_t workspace_bytes, 
   p.n_mtiles = static_cast<int>(ceil_div64(a->sq, 128));
   p.n_ntiles = static_cast<int>(ceil_div64(a->skv, 128));
   p.sq_pad = p.n_mtiles * 128;
+  {
+    // dQ grid: as many (batch, query head) pairs per group as keep their K and V
+    // within about 32 MiB (a quarter of L2), whole KV-head groups where possible
+    const int64_t kv_bytes_per_kv_head = 2 * static_cast<int64_t>(a->skv) * a->d * 2;
+    const int g = a->hq / a->hkv;
+    int64_t heads = kv_bytes_per_kv_head > 0 ? (int64_t{32} << 20) / kv_bytes_per_kv_head * g : g;
+    heads = heads < g ? g : heads - heads % g;
+    const int64_t bh = static_cast<int64_t>(a->b) * a->hq;
+    p.head_group = static_cast<int>(heads > bh ? bh : heads);
+  }
   p.causal = c.causal;
   p.off = c.off;
   p.local = c.local;

@@ -215,9 +215,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // longest row tiles first (causal: the last tiles see the most keys)
-  const int bh = blockIdx.x % (p.b * p.hq);
-  const int m = p.n_mtiles - 1 - static_cast<int>(blockIdx.x / (p.b * p.hq));
+  // Longest row tiles first (causal: the last tiles see the most keys), within
+  // groups of head_group consecutive (batch, query head) pairs taken one group
+  // after the other: the CTAs in flight then read the K / V of a few heads only,
+  // which stay in L2 (longest first over every head at once kept all of them in
+  // flight and re-read K / V from DRAM); the hardware hands the next CTA to the
+  // first SM that frees, so each group is balanced as the whole grid was.
+  const int BH = p.b * p.hq;
+  const int per_group = p.head_group * p.n_mtiles;
+  const int g0 = static_cast<int>(blockIdx.x / per_group) * p.head_group;
+  const int gsize = min(p.head_group, BH - g0);
+  const int r_in = static_cast<int>(blockIdx.x % per_group);
+  const int bh = g0 + r_in % gsize;
+  const int m = p.n_mtiles - 1 - r_in / gsize;
   const int h = bh % p.hq, bi = bh / p.hq, kvh = h / p.g;
   const int row0 = m * BM;
   int n_lo, n_hi;

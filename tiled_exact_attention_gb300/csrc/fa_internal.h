@@ -126,6 +126,7 @@ struct BwdParams {
   int n_mtiles, n_ntiles;  // 128-row query tiles, 128-key blocks
   int* status;
   float sc_k, sc_b;     // softcap as in PrefillParams (sc_b = 0: off)
+  int head_group;       // dQ grid: (batch, query head) pairs whose row tiles are interleaved, longest first
 };
 
 // e4m3 quantisation of one [b][s][h][d] tensor.
