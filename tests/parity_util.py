@@ -70,3 +70,31 @@ def assert_parity(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
 
 def default_scale(d):
     return 1.0 / math.sqrt(d)
+
+
+def e4m3_rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale):
+    """Per-element bound of what rounding P to e4m3 (and O to bf16) may change in the
+    8-bit forward pass, every term from the oracle on the dequantised inputs:
+
+      |O_ic - O_ref,ic| <= 2^-4 * sum_j P_ij |V_jc|               (normal e4m3 codes)
+                         + 2^-10 * Pmax_i * sum_{j visible} |V_jc|  (subnormal codes)
+                         + 2^-8 * |O_ref,ic| + 1e-6                (bf16 O, fp32 sums)
+
+    The kernel forms p_j = 2^(x_j - m_ref) with a reference maximum no larger than
+    the row's maximum, so its largest p is at least 1 and its row sum l at least
+    1 / Pmax_i, Pmax_i = exp(m_i - LSE_i); a normal code (p >= 2^-6) is off by at most
+    2^-4 of p, a subnormal one by at most 2^-10.  sum_j P_ij |V_jc| is the oracle with
+    |V| in place of V; the visible sum of |V| is the oracle at scale 0 (uniform weights
+    1 / n_i, LSE = ln n_i) times n_i; m_i is bounded above by LSE at 1000 times the
+    scale, divided by 1000."""
+    win = window if window else (-1, -1)
+    kw = dict(causal=causal, q_pos_offset=off, rows=rows, window=win)
+    a_abs, _ = oracle.attention(qx, kx, np.abs(vx), scale=scale, **kw)
+    mean_abs, l0 = oracle.attention(qx, kx, np.abs(vx), scale=0.0, **kw)
+    _, l_big = oracle.attention(qx, kx, vx, scale=1000.0 * scale, **kw)
+    vis = ~np.isneginf(l_ref)
+    b_abs = np.zeros_like(mean_abs)
+    b_abs[vis] = mean_abs[vis] * np.exp(l0[vis])[:, None]
+    pmax = np.zeros_like(l_ref)
+    pmax[vis] = np.minimum(1.0, np.exp(l_big[vis] / 1000.0 - l_ref[vis]))
+    return 2.0 ** -4 * a_abs + 2.0 ** -10 * pmax[:, None] * b_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-6

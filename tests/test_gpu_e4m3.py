@@ -34,6 +34,7 @@ import torch
 
 import oracle
 from oracle import e4m3
+from parity_util import e4m3_rounding_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -84,22 +85,6 @@ CASES = [
 ]
 
 
-def rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale):
-    """Per-element bound of what rounding P to e4m3 and O to bf16 may change (see the module docstring);
-    every term from the oracle on the dequantised inputs."""
-    win = window if window else (-1, -1)
-    kw = dict(causal=causal, q_pos_offset=off, rows=rows, window=win)
-    a_abs, _ = oracle.attention(qx, kx, np.abs(vx), scale=scale, **kw)          # sum_j P_ij |V_j|
-    mean_abs, l0 = oracle.attention(qx, kx, np.abs(vx), scale=0.0, **kw)        # uniform weights, LSE = ln n_i
-    _, l_big = oracle.attention(qx, kx, vx, scale=1000.0 * scale, **kw)        # LSE_1000 / 1000 >= m_i
-    vis = ~np.isneginf(l_ref)
-    b_abs = np.zeros_like(mean_abs)
-    b_abs[vis] = mean_abs[vis] * np.exp(l0[vis])[:, None]                       # sum_{j visible} |V_j|
-    pmax = np.zeros_like(l_ref)
-    pmax[vis] = np.minimum(1.0, np.exp(l_big[vis] / 1000.0 - l_ref[vis]))
-    return 2.0 ** -4 * a_abs + 2.0 ** -10 * pmax[:, None] * b_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-6
-
-
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(str(x) for x in c))
 def test_e4m3_forward_matches_oracle_on_dequantised_inputs(case):
     b, sq, skv, hq, hkv, causal, off, window, vmean = case
@@ -124,7 +109,7 @@ def test_e4m3_forward_matches_oracle_on_dequantised_inputs(case):
     masked = np.isneginf(l_ref)
     assert np.all(np.isneginf(lg[masked])) and np.all(og[masked] == 0.0)
     vis = ~masked
-    tol = rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale)
+    tol = e4m3_rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale)
     err = np.abs(og - o_ref)
     worst = np.unravel_index(np.argmax(err[vis] - tol[vis]), err[vis].shape)
     assert np.all(err[vis] <= tol[vis]), (

@@ -1,6 +1,7 @@
 """Pins of the e4m3 reference (oracle/e4m3.py) to the published format: known codes,
 round trips of every finite code, ties to even, saturation, and the block scales."""
 import numpy as np
+import pytest
 
 from oracle import e4m3
 
@@ -51,3 +52,93 @@ def test_block_scales_and_bounds():
     assert ds_h.shape == (2, 3)
     np.testing.assert_allclose(e4m3.dequantize_blocks(codes_h, ds_h, per_head=True), x,
                                atol=float(np.abs(x).max()) / 16)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_block_scales_at_every_head_width(d):
+    """One scale per 128 rows of one (batch, head), whatever the head width."""
+    rng = np.random.default_rng(d)
+    x = (rng.standard_normal((1, 257, 2, d)) * 3.0).astype(np.float32)
+    codes, ds = e4m3.quantize_blocks(x)
+    assert codes.shape == x.shape and ds.shape == (1, 2, 3)
+    for h in range(2):
+        for k, (r0, r1) in enumerate(((0, 128), (128, 256), (256, 257))):
+            assert ds[0, h, k] == np.float32(np.abs(x[0, r0:r1, h, :]).max()) / np.float32(448)
+            assert np.abs(e4m3.decode(codes[0, r0:r1, h, :])).max() == 448.0
+
+
+def _model_e4m3_forward(qx, kx, vx, scale, causal, off, window):
+    """A step-by-step fp64 model of what rounding P to e4m3 does in the 8-bit forward pass:
+    per row, key blocks of 128 from the highest, the reference maximum moved only when a
+    block's maximum exceeds it by more than 8 log2 units, p = 2^(x - m_ref) rounded to e4m3
+    for the P V product, l summed from the unrounded p, O = o / l rounded to bf16."""
+    import torch
+
+    b, sq, hq, d = qx.shape
+    skv, hkv = kx.shape[1], kx.shape[2]
+    g = hq // hkv
+    wl, wr = window
+    out = np.zeros((b * hq * sq, d))
+    r = 0
+    for bi in range(b):
+        for h in range(hq):
+            for i in range(sq):
+                x = kx[bi, :, h // g, :] @ qx[bi, i, h, :] * scale / np.log(2.0)
+                j = np.arange(skv)
+                vis = np.ones(skv, dtype=bool)
+                if causal:
+                    vis &= j <= i + off
+                if wl >= 0:
+                    vis &= j >= i + off - wl
+                if wr >= 0:
+                    vis &= j <= i + off + wr
+                x = np.where(vis, x, -np.inf)
+                m_ref, l, o = -np.inf, 0.0, np.zeros(d)
+                for n in range((skv + 127) // 128 - 1, -1, -1):
+                    blk = x[n * 128:(n + 1) * 128]
+                    bm = blk.max()
+                    if bm > m_ref + 8:
+                        alpha = 2.0 ** (m_ref - bm) if np.isfinite(m_ref) else 0.0
+                        o, l, m_ref = o * alpha, l * alpha, bm
+                    if not np.isfinite(m_ref):
+                        continue
+                    p = 2.0 ** (blk - m_ref)
+                    pr = e4m3.decode(e4m3.encode(p.astype(np.float32)))
+                    l += p.sum()
+                    o += pr @ vx[bi, n * 128:n * 128 + len(blk), h // g, :]
+                if l > 0:
+                    out[r] = torch.tensor(o / l).to(torch.bfloat16).double().numpy()
+                r += 1
+    return out
+
+
+@pytest.mark.parametrize("d,causal,window,vmean", [
+    (64, True, None, 0.0), (128, False, (60, 10), 0.0), (256, True, None, 1.5), (64, False, None, -2.0),
+])
+def test_rounding_bound_holds_for_a_model_of_p_rounding(d, causal, window, vmean):
+    """The tolerance of the GPU e4m3 check (parity_util.e4m3_rounding_bound, every term from
+    the oracle) bounds the model above on causal, windowed and shifted-V inputs at every head
+    width, and stays tight enough that a doubled O would fail it on shifted-V inputs."""
+    from parity_util import e4m3_rounding_bound
+
+    import oracle
+
+    rng = np.random.default_rng(d + (7 if causal else 0))
+    b, sq, skv, hq, hkv = 1, 150, 300, 2, 1
+    x = lambda *shape: rng.standard_normal(shape).astype(np.float32)  # noqa: E731
+    q, k, v = x(b, sq, hq, d), x(b, skv, hkv, d), x(b, skv, hkv, d) + np.float32(vmean)
+    qx = e4m3.dequantize_blocks(*e4m3.quantize_blocks(q))
+    kx = e4m3.dequantize_blocks(*e4m3.quantize_blocks(k))
+    vc, vd = e4m3.quantize_blocks(v, per_head=True)
+    vx = e4m3.dequantize_blocks(vc, vd, per_head=True)
+    scale = 1.0 / np.sqrt(d)
+    off = skv - sq
+    rows = oracle.all_rows(b, hq, sq)
+    o_ref, l_ref = oracle.attention(qx, kx, vx, causal=causal, q_pos_offset=off, scale=scale, rows=rows,
+                                    window=window if window else (-1, -1))
+    tol = e4m3_rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale)
+    model = _model_e4m3_forward(qx, kx, vx, scale, causal, off, window if window else (-1, -1))
+    vis = ~np.isneginf(l_ref)
+    assert np.all(np.abs(model[vis] - o_ref[vis]) <= tol[vis])
+    if vmean:
+        assert np.mean(np.abs(o_ref[vis]) > tol[vis]) > 0.9
