@@ -19,7 +19,7 @@ rank's time.
 Every roofline divides by the measured burst bf16 GEMM peak (each launch lasts
 well under a millisecond, between L2 flushes); the sustained peak is reported
 beside it.  `--only NAME[,NAME...]` times just the named lines (prefill, decode,
-gqa_long, ragged_d64, ragged_d256, backward, e4m3, paged, variants, e2e, link)
+gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, paged, variants, e2e, link)
 and prints them as one JSON object: the form the ncu captures use.
 """
 from __future__ import annotations
@@ -204,7 +204,8 @@ def _setup(args):
     return ws, rank, dev, flush
 
 
-SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "backward", "e4m3", "variants", "e2e", "link")
+SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "backward", "e4m3", "e4m3_d64", "variants", "e2e",
+             "link")
 
 
 def run_only(args):
@@ -227,6 +228,8 @@ def run_only(args):
             out[nm] = bench_backward(dev, flush, steps=steps, warmup=args.warmup)
         elif nm == "e4m3":
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup)
+        elif nm == "e4m3_d64":
+            out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup, workload="ragged_" + nm[5:])
         elif nm == "variants":
             out[nm] = bench_variants(dev, flush, steps=steps)
         elif nm in ("e2e", "link"):
@@ -332,6 +335,7 @@ def run_ours(args):
     paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
     bwd = bench_backward(dev, flush, steps=few)
     e4m3 = bench_e4m3(dev, flush, steps=max(10, min(200, K // 25)))
+    e4m3_rag = {f"e4m3_d{w}": bench_e4m3(dev, flush, steps=few, workload=f"ragged_d{w}") for w in (64,)}
     variants = bench_variants(dev, flush, steps=few)
 
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
@@ -359,6 +363,10 @@ def run_ours(args):
     e4["roofline"] = _tensor_roofline(e4m3["value"], kernel=e4m3["kernel"],
                                       traffic=_profiled_traffic("fa_prefill_kernel_e4m3"), ratio=2.0,
                                       dtype_note=" x 2 (the nominal fp8 : bf16 ratio)")
+    for key, val in e4m3_rag.items():
+        val["roofline"] = _tensor_roofline(val["value"], kernel=val["kernel"], ratio=2.0,
+                                           traffic=_profiled_traffic("fa_prefill_kernel_" + key),
+                                           dtype_note=" x 2 (the nominal fp8 : bf16 ratio)")
     bw = dict(bwd)
     bw["roofline"] = _tensor_roofline(bwd["value"], kernel="fa_bwd_dkdv_kernel (the larger of the two product kernels)",
                                       traffic=_profiled_traffic("fa_bwd_dkdv_kernel"))
@@ -403,6 +411,7 @@ def run_ours(args):
                                               "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
                                               "peak_source": f"{peak_src} copy bandwidth", "traffic": None}),
         "e4m3": e4,
+        "e4m3_d64": e4m3_rag["e4m3_d64"],
         "backward": bw,
         "variants": variants,
         "roofline": dict(_tensor_roofline(per_gpu_tflops, kernel="fa_prefill_kernel<128, bf16>", traffic=pre_traffic),
@@ -559,22 +568,25 @@ def bench_backward(dev, flush, steps=30, warmup=3):
             "kernels": "fa_bwd_pre_kernel + fa_bwd_dq_kernel + fa_bwd_dkdv_kernel", "steps": steps}
 
 
-def bench_e4m3(dev, flush, steps=30, warmup=3):
-    """The 8-bit forward pass (fa_fwd_e4m3) on the causal-prefill workload, its inputs quantised once
-    outside the timed region (fa_quantize_e4m3: per-block Q, K scales; V transposed, per-head scale)."""
+def bench_e4m3(dev, flush, steps=30, warmup=3, workload="causal_prefill"):
+    """The 8-bit forward pass (fa_fwd_e4m3) on a forward workload (the causal prefill, or a ragged-tail
+    d = 64 / d = 256 one), its inputs quantised once outside the timed region (fa_quantize_e4m3:
+    per-block Q, K scales; V transposed, per-head scale)."""
     import torch
 
     from tiled_exact_attention_gb300 import fa_fwd_e4m3, fa_sync_status, quantize_qkv_e4m3
     from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
 
-    w = WORKLOADS["causal_prefill"]
+    w = WORKLOADS[workload]
     q, k, v = (t.to(dev) for t in make_qkv(w))
     (q8, qd), (k8, kd), (vt8, vd) = quantize_qkv_e4m3(q, k, v)
-    o = torch.empty_like(q)
+    del k, v
+    o = torch.empty((w.b, w.sq, w.hq, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.b, w.hq, w.sq), dtype=torch.float32, device=dev)
+    off = w.offset if w.causal else None
 
     def step():
-        fa_fwd_e4m3(q8, qd, k8, kd, vt8, vd, causal=True, q_pos_offset=w.offset, out=o, lse=lse)
+        fa_fwd_e4m3(q8, qd, k8, kd, vt8, vd, causal=w.causal, q_pos_offset=off, out=o, lse=lse)
 
     for _ in range(warmup):
         flush.zero_()
@@ -594,8 +606,9 @@ def bench_e4m3(dev, flush, steps=30, warmup=3):
     flops = 4.0 * w.d * w.visible_pairs_per_head() * w.b * w.hq
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "dtype": "e4m3 inputs, e4m3 P, fp32 accumulation, bf16 O",
-            "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "causal": True},
-            "flops_per_launch": flops, "kernel": "fa_prefill_kernel<128, bf16, dense, e4m3>", "steps": steps}
+            "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "causal": w.causal,
+                       "inputs": f"{w.dtype} std {w.std}, quantised outside the timed region"},
+            "flops_per_launch": flops, "kernel": f"fa_prefill_kernel<{w.d}, bf16, dense, e4m3>", "steps": steps}
 
 
 def _timed(step, flush, steps, warmup=3):

@@ -337,7 +337,7 @@ fa_status fa_bwd(const fa_bwd_args* args, void* workspace, size_t workspace_byte
  * precision and hardware": FP8 as an extra speed path, a scale factor per block,
  * the scales carried into the computation, softmax statistics kept in fp32).
  *
- * fa_quantize_e4m3 turns one bf16 / fp16 tensor [b, s, h, d] (d in {64, 128})
+ * fa_quantize_e4m3 turns one bf16 / fp16 tensor [b, s, h, d] (d in {64, 128, 256})
  * into e4m3 codes: descale = amax / 448 over each 128-row block of one (batch,
  * head) (per_head = 0; descale [b, h, ceil(s / 128)]) or over the whole (batch,
  * head) (per_head = 1; descale [b, h]); code = round-to-nearest-even e4m3 of
@@ -362,7 +362,7 @@ typedef struct {
 fa_status fa_quantize_e4m3(const fa_quant_args* args, void* stream);
 
 /*
- * Forward pass with e4m3 Q, K, V (d = 128): S = (Q8 K8^T) * q_descale[tile of
+ * Forward pass with e4m3 Q, K, V (d in {64, 128}; FA_ERR_UNSUPPORTED otherwise): S = (Q8 K8^T) * q_descale[tile of
  * 128 rows] * k_descale[block of 128 keys] * scale, P = exp(S - m) rounded to e4m3
  * for the P V product (P <= 2^8 by the lazy-rescale rule, within e4m3's range),
  * row max and sum in fp32, O = (P8 V8) * v_descale[head] / l written as bf16,

@@ -295,7 +295,7 @@ def test_e4m3_validation(lib):
     qa.x = qa.out = qa.descale = 4096
     qa.x_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
     qa.out_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
-    for field, value, expect in (("d", 256, 2), ("d", 96, 2), ("transpose", 2, 1), ("x", 0, 1), ("out", 4104, 1)):
+    for field, value, expect in (("d", 512, 2), ("d", 96, 2), ("transpose", 2, 1), ("x", 0, 1), ("out", 4104, 1)):
         old = getattr(qa, field)
         setattr(qa, field, value)
         assert lib.fa_quantize_e4m3(ctypes.byref(qa), None) == expect, field
@@ -310,7 +310,7 @@ def test_e4m3_validation(lib):
         setattr(a, f, (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128))
     a.o_strides = (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128)
     a.scale = 0.1
-    for field, value, expect in (("d", 64, 2), ("d", 256, 2), ("vt", 0, 1), ("v_descale", 0, 1), ("causal", 3, 1),
+    for field, value, expect in (("d", 96, 2), ("d", 256, 2), ("vt", 0, 1), ("v_descale", 0, 1), ("causal", 3, 1),
                                  ("scale", 0.0, 1), ("hq", 3, 1)):
         old = getattr(a, field)
         setattr(a, field, value)

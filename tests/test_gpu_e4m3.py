@@ -56,6 +56,9 @@ def _f32(t):
     ((1, 257, 2, 64), "fp16", False, False),
     ((2, 300, 3, 128), "bf16", True, True),
     ((1, 129, 4, 128), "fp16", True, True),
+    ((1, 300, 2, 256), "bf16", False, False),
+    ((2, 200, 2, 256), "fp16", True, True),
+    ((1, 140, 3, 64), "bf16", True, True),
 ])
 def test_quantizer_matches_reference_code_for_code(shape, dts, per_head, transpose):
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dts]
@@ -74,21 +77,24 @@ def test_quantizer_matches_reference_code_for_code(shape, dts, per_head, transpo
 
 
 CASES = [
-    # b, sq, skv, hq, hkv, causal, offset, window, V mean
-    (1, 513, 513, 2, 2, True, None, None, 0.0),
-    (2, 300, 700, 4, 2, False, None, None, 0.0),
-    (1, 640, 640, 8, 2, True, None, None, 0.0),
-    (1, 400, 400, 2, 1, False, None, (100, 20), 0.0),
-    (1, 200, 100, 2, 2, True, 50, None, 0.0),
-    (2, 300, 700, 4, 2, False, None, None, 1.5),
-    (1, 640, 640, 4, 4, True, None, None, -2.0),
+    # b, sq, skv, hq, hkv, d, causal, offset, window, V mean
+    (1, 513, 513, 2, 2, 128, True, None, None, 0.0),
+    (2, 300, 700, 4, 2, 128, False, None, None, 0.0),
+    (1, 640, 640, 8, 2, 128, True, None, None, 0.0),
+    (1, 400, 400, 2, 1, 128, False, None, (100, 20), 0.0),
+    (1, 200, 100, 2, 2, 128, True, 50, None, 0.0),
+    (2, 300, 700, 4, 2, 128, False, None, None, 1.5),
+    (1, 640, 640, 4, 4, 128, True, None, None, -2.0),
+    (1, 513, 513, 2, 2, 64, True, None, None, 0.0),
+    (2, 300, 700, 4, 2, 64, False, None, None, 1.5),
+    (1, 400, 400, 2, 1, 64, False, None, (100, 20), 0.0),
+    (1, 640, 640, 8, 2, 64, True, None, None, -2.0),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(str(x) for x in c))
 def test_e4m3_forward_matches_oracle_on_dequantised_inputs(case):
-    b, sq, skv, hq, hkv, causal, off, window, vmean = case
-    d = 128
+    b, sq, skv, hq, hkv, d, causal, off, window, vmean = case
     q, k, v = make_custom(b, sq, skv, hq, hkv, d, "bf16", std=1.0, seed=zlib.crc32(repr(case).encode()) % 100000)
     if vmean:
         v = (v.float() + vmean).to(torch.bfloat16)
@@ -119,3 +125,14 @@ def test_e4m3_forward_matches_oracle_on_dequantised_inputs(case):
     if vmean:
         # the bound is tight enough to see a V scale applied twice (O doubled) or not at all
         assert np.mean(np.abs(o_ref[vis]) > tol[vis]) > 0.9
+
+
+def test_e4m3_forward_rejects_d256():
+    """d = 256 is not offered on the 8-bit path (the 16-bit path serves it)."""
+    from tiled_exact_attention_gb300._lib import FaError
+
+    q, k, v = make_custom(1, 128, 128, 1, 1, 256, "bf16", seed=3)
+    (q8, qd), (k8, kd), (vt8, vd) = (fa_quantize_e4m3(q.to(DEV)), fa_quantize_e4m3(k.to(DEV)),
+                                     fa_quantize_e4m3(v.to(DEV), per_head=True, transpose=True))
+    with pytest.raises(FaError):
+        fa_fwd_e4m3(q8, qd, k8, kd, vt8, vd)

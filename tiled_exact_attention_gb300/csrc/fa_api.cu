@@ -142,6 +142,7 @@ bool encode_map(CUtensorMap* m, const void* ptr, fa_dtype dt, int d, int h, int 
 
 // General 4-D map over one-byte elements: dims innermost first, strides in bytes
 // of dims 1..3, the given box, 128-byte swizzle.
+// Box rows of box_in[0] bytes: the 128-byte swizzle, or the 64-byte one for 64-byte rows.
 bool encode_map_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], const int64_t strides_b[3],
                    const uint32_t box_in[4]) {
   EncodeTiledFn enc = encode_fn();
@@ -152,8 +153,9 @@ bool encode_map_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], c
                            static_cast<cuuint64_t>(strides_b[2])};
   cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
   cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = box_in[0] == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1051,7 +1053,7 @@ fa_status validate_quant(const fa_quant_args* a) {
   if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
   if (a->b < 1 || a->s < 0 || a->h < 1) return FA_ERR_INVALID_ARG;
   if ((a->transpose != 0 && a->transpose != 1) || (a->per_head != 0 && a->per_head != 1)) return FA_ERR_INVALID_ARG;
-  if (a->d != 64 && a->d != 128) return FA_ERR_UNSUPPORTED;
+  if (a->d != 64 && a->d != 128 && a->d != 256) return FA_ERR_UNSUPPORTED;
   if (a->s > (1 << 30)) return FA_ERR_UNSUPPORTED;
   if (a->s == 0) return FA_OK;
   if (a->x == nullptr || a->out == nullptr || a->descale == nullptr) return FA_ERR_INVALID_ARG;
@@ -1119,7 +1121,8 @@ fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* a, void* stream) {
     const uint64_t qd[4] = {static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hq), static_cast<uint64_t>(a->sq),
                             static_cast<uint64_t>(a->b)};
     const int64_t qs[3] = {a->q_strides[2], a->q_strides[1], a->q_strides[0]};
-    const uint32_t box[4] = {static_cast<uint32_t>(a->d), 1, 128, 1};  // one 128-row tile, 128 bytes per row
+    // one 128-row tile in chunks of up to 128 bytes per row (64 for d = 64)
+    const uint32_t box[4] = {static_cast<uint32_t>(a->d < 128 ? a->d : 128), 1, 128, 1};
     if (!encode_map_u8(&p.tm_q, a->q, qd, qs, box)) return FA_ERR_INVALID_ARG;
   }
   if (a->skv > 0) {
@@ -1130,7 +1133,7 @@ fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* a, void* stream) {
     const uint64_t vd[4] = {static_cast<uint64_t>(a->skv), static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hkv),
                             static_cast<uint64_t>(a->b)};
     const int64_t vs[3] = {a->vt_strides[2], a->vt_strides[1], a->vt_strides[0]};
-    const uint32_t kbox[4] = {static_cast<uint32_t>(a->d), 1, 128, 1};
+    const uint32_t kbox[4] = {static_cast<uint32_t>(a->d < 128 ? a->d : 128), 1, 128, 1};
     const uint32_t vbox[4] = {128, static_cast<uint32_t>(a->d), 1, 1};  // 128 keys of every d-row
     if (!encode_map_u8(&p.tm_k, a->k, kd, ks, kbox) || !encode_map_u8(&p.tm_v, a->vt, vd, vs, vbox))
       return FA_ERR_INVALID_ARG;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) fa_descale_kernel(float* slots, int64_t n
 // One CTA of 256 threads per 128-row block of one (batch, head).
 template <bool BF16, bool TRANSPOSE>
 __global__ void __launch_bounds__(256) fa_quant_kernel(const __grid_constant__ QuantParams p) {
-  __shared__ __align__(16) uint8_t tile[128 * 128 + 16];  // transposed: [d][128 rows]
+  __shared__ __align__(16) uint8_t tile[256 * 128 + 16];  // transposed: [d][128 rows], d <= 256
   const int blk = blockIdx.x % p.nblk;
   const int bh = blockIdx.x / p.nblk;
   const int h = bh % p.h, bi = bh / p.h;

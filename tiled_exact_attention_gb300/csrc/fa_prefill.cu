@@ -39,10 +39,16 @@ struct Cfg {
   static constexpr int ELT = E8 ? 1 : 2;             // bytes per input element
   static constexpr int BM = 128;                     // rows per Q tile (= TMEM lanes)
   static constexpr int NQ = (D <= 128) ? 2 : 1;      // Q tiles per CTA
-  static constexpr int BN = (D <= 128) ? 128 : 64;   // keys per K/V block
-  static constexpr int STAGES = (E8 || D == 64) ? 8 : 4;  // K/V ring slots
-  static constexpr int DC = D * ELT / 128;           // 128-byte chunks per row
-  static constexpr int CHUNK_ELEMS = 128 / ELT;      // elements per chunk
+  // keys per K/V block (e4m3: 128, so that a row of the transposed V tile is 128 bytes)
+  static constexpr int BN = (D <= 128 || E8) ? 128 : 64;
+  static constexpr int STAGES = E8 ? (D == 256 ? 4 : 8) : (D == 64 ? 8 : 4);  // K/V ring slots
+  // Q and K rows are staged in swizzle chunks of CHUNK_BYTES: 128-byte rows with the
+  // 128-byte swizzle, or (e4m3, d = 64) one 64-byte chunk with the 64-byte swizzle
+  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr int CHUNK_BYTES = ROW_BYTES < 128 ? ROW_BYTES : 128;
+  static constexpr bool SW64 = CHUNK_BYTES == 64;
+  static constexpr int DC = ROW_BYTES / CHUNK_BYTES;     // chunks per row
+  static constexpr int CHUNK_ELEMS = CHUNK_BYTES / ELT;  // elements per chunk
   static constexpr int Q_BYTES = BM * D * ELT;
   static constexpr int KV_BYTES = BN * D * ELT;
   // softmax warpgroups + one control warpgroup (producer, MMA issuer, two idle
@@ -202,7 +208,7 @@ __device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p
 template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool E8, bool W>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int t, int slot) {
   if constexpr (E8)
-    issue_s_tile_e4m3<D, BN, BM, Q_BYTES, KV_BYTES, ID, W>(d_tmem, q_desc, k_desc, t, slot);
+    issue_s_tile_e4m3<D, BN, BM, Q_BYTES, KV_BYTES, ID, W, (D < 128 ? D : 128)>(d_tmem, q_desc, k_desc, t, slot);
   else
     issue_s_tile<D, BN, BM, Q_BYTES, KV_BYTES, ID, W>(d_tmem, q_desc, k_desc, t, slot);
 }
@@ -333,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
           if (w.n_hi[t] > w.n_lo_t[t]) {
 #pragma unroll
             for (int c = 0; c < C::DC; ++c)
-              tma_load_4d(smem + t * C::Q_BYTES + c * (BM * 128), &p.tm_q, q_full, c * C::CHUNK_ELEMS, w.h,
+              tma_load_4d(smem + t * C::Q_BYTES + c * (BM * C::CHUNK_BYTES), &p.tm_q, q_full, c * C::CHUNK_ELEMS, w.h,
                           w.q_base + (w.m_cta * NQ + t) * BM, w.tb);
           }
         }
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             const CUtensorMap* map = (L & 1) ? &p.tm_v : &p.tm_k;
 #pragma unroll
             for (int c = 0; c < C::DC; ++c)
-              tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * 128), map, &kv_full[slot], c * C::CHUNK_ELEMS,
+              tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * C::CHUNK_BYTES), map, &kv_full[slot], c * C::CHUNK_ELEMS,
                                w.kvh, w.k_base + n * BN, w.tbk, pol_kv);
           }
         }
@@ -419,8 +425,9 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       // Descriptors are built once; per slot, tile and K step only the start
       // address field (low bits, address >> 4) moves, by compile-time amounts.
       const uint32_t ring_s = smem_u32(ring);
-      const uint64_t q_desc = sdesc_sw128(smem_u32(smem), 16, 1024);  // Q tile 0, K step 0
-      const uint64_t k_desc = sdesc_sw128(ring_s, 16, 1024);          // slot 0 read as K (K-major)
+      // Q tile 0 and slot 0 read as K (K-major), K step 0
+      const uint64_t q_desc = C::SW64 ? sdesc_sw64(smem_u32(smem), 16, 512) : sdesc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t k_desc = C::SW64 ? sdesc_sw64(ring_s, 16, 512) : sdesc_sw128(ring_s, 16, 1024);
       // slot 0 read as V: MN-major (16-bit), or K-major V^T (e4m3)
       const uint64_t v_desc = E8 ? sdesc_sw128(ring_s, 16, 1024) : sdesc_sw128(ring_s, BN * 128, 1024);
       uint32_t gL = 0, q_uses = 0;
@@ -867,12 +874,14 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-bool prefill_e4m3_supported(int d) { return d == 128; }
+// (d = 256 is not offered: its two-chunk 8-bit S product measured all zeros on the
+// GPU, a cause not found; the 16-bit path serves d = 256)
+bool prefill_e4m3_supported(int d) { return d == 64 || d == 128; }
 
-cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stream) {
-  if (d != 128 || p.cu_q != nullptr || p.num_splits != 1) return cudaErrorInvalidValue;
-  using C = Cfg<128, true>;
-  auto kern = fa_prefill_kernel<128, true, false, true>;
+template <int D>
+cudaError_t launch_e4m3_t(const PrefillParams& p, cudaStream_t stream) {
+  using C = Cfg<D, true>;
+  auto kern = fa_prefill_kernel<D, true, false, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long items = static_cast<long long>(p.n_mcta) * p.b * p.hq;
@@ -881,6 +890,15 @@ cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stre
   const long long grid = items < p.max_ctas ? items : p.max_ctas;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stream) {
+  if (p.cu_q != nullptr || p.num_splits != 1) return cudaErrorInvalidValue;
+  switch (d) {
+    case 64: return launch_e4m3_t<64>(p, stream);
+    case 128: return launch_e4m3_t<128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int prefill_block_n(int d) { return d <= 128 ? 128 : 64; }

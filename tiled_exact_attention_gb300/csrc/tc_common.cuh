@@ -129,18 +129,21 @@ __device__ __forceinline__ void issue_pv_tile(uint32_t o_tmem, uint32_t p_tmem, 
 }
 
 
-// 8-bit forms: S = Q K^T with e4m3 operands (D / 32 MMAs of K = 32, same 128-byte
-// swizzled K-major layout: a 128-byte row holds 128 elements) ...
-template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool W = false>
+// 8-bit forms: S = Q K^T with e4m3 operands (D / 32 MMAs of K = 32, K-major rows
+// staged in swizzle chunks of CB bytes: 128-byte chunks with the 128-byte swizzle,
+// or for d = 64 one 64-byte chunk with the 64-byte swizzle; a K step of 32 elements
+// advances the start address by 32 bytes inside the chunk) ...
+template <int D, int BN, int BM, int Q_BYTES, int KV_BYTES, uint32_t ID, bool W = false, int CB = 128>
 __device__ __forceinline__ void issue_s_tile_e4m3(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, int q_slot,
                                                   int slot) {
   uint64_t qd = q_desc + static_cast<uint32_t>((q_slot * Q_BYTES) >> 4);
   uint64_t kd = k_desc + static_cast<uint32_t>((slot * KV_BYTES) >> 4);
   asm volatile("" : "+l"(qd), "+l"(kd));
+  constexpr int SPC = CB / 32;  // K steps per chunk
 #pragma unroll
   for (int k = 0; k < D / 32; ++k) {
-    const uint32_t offa = static_cast<uint32_t>(((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4);
-    const uint32_t offb = static_cast<uint32_t>(((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4);
+    const uint32_t offa = static_cast<uint32_t>(((k / SPC) * (BM * CB) + (k % SPC) * 32) >> 4);
+    const uint32_t offb = static_cast<uint32_t>(((k / SPC) * (BN * CB) + (k % SPC) * 32) >> 4);
     umma_ss_f8<W>(d_tmem, qd + offa, kd + offb, ID, k > 0 ? 1u : 0u);
   }
 }
