@@ -19,7 +19,8 @@ rank's time.
 Every roofline divides by the measured burst bf16 GEMM peak (each launch lasts
 well under a millisecond, between L2 flushes); the sustained peak is reported
 beside it.  `--only NAME[,NAME...]` times just the named lines (prefill, decode,
-gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, paged, variants, e2e, link)
+gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, paged, decode_e4m3, variants, e2e,
+link)
 and prints them as one JSON object: the form the ncu captures use.
 """
 from __future__ import annotations
@@ -204,8 +205,8 @@ def _setup(args):
     return ws, rank, dev, flush
 
 
-SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "backward", "e4m3", "e4m3_d64", "variants", "e2e",
-             "link")
+SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "decode_e4m3", "backward", "e4m3", "e4m3_d64",
+             "variants", "e2e", "link")
 
 
 def run_only(args):
@@ -228,6 +229,8 @@ def run_only(args):
             out[nm] = bench_backward(dev, flush, steps=steps, warmup=args.warmup)
         elif nm == "e4m3":
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup)
+        elif nm == "decode_e4m3":
+            out[nm] = bench_decode_e4m3(dev, flush, steps=steps, warmup=args.warmup)
         elif nm == "e4m3_d64":
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup, workload="ragged_" + nm[5:])
         elif nm == "variants":
@@ -333,6 +336,7 @@ def run_ours(args):
     configs = {nm: bench_config(dev, flush, WORKLOADS[nm], steps=few) for nm in ("gqa_long", "ragged_d64",
                                                                                  "ragged_d256")}
     paged = bench_paged_decode(dev, flush, steps=max(20, min(500, K // 10)))
+    dec8 = bench_decode_e4m3(dev, flush, steps=max(20, min(500, K // 10)))
     bwd = bench_backward(dev, flush, steps=few)
     e4m3 = bench_e4m3(dev, flush, steps=max(10, min(200, K // 25)))
     e4m3_rag = {f"e4m3_d{w}": bench_e4m3(dev, flush, steps=few, workload=f"ragged_d{w}") for w in (64,)}
@@ -410,6 +414,7 @@ def run_ours(args):
         "decode_paged": dict(paged, roofline={"bound": "hbm", "achieved": paged["value"], "peak": hbm,
                                               "unit": "GB/s", "frac": round(paged["value"] / hbm, 4),
                                               "peak_source": f"{peak_src} copy bandwidth", "traffic": None}),
+        "decode_e4m3": dec8,
         "e4m3": e4,
         "e4m3_d64": e4m3_rag["e4m3_d64"],
         "backward": bw,
@@ -609,6 +614,47 @@ def bench_e4m3(dev, flush, steps=30, warmup=3, workload="causal_prefill"):
             "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "causal": w.causal,
                        "inputs": f"{w.dtype} std {w.std}, quantised outside the timed region"},
             "flops_per_launch": flops, "kernel": f"fa_prefill_kernel<{w.d}, bf16, dense, e4m3>", "steps": steps}
+
+
+def bench_decode_e4m3(dev, flush, steps=30, warmup=3):
+    """Split-KV decode over e4m3 K and V (fa_fwd_splitkv_e4m3) on the decode workload's shape (B=8, Hq=32,
+    Hkv=8, KV=32768, d=128, the same seeded values quantised outside the timed region: K with one scale per
+    128 keys, V with one per head); KV GB/s of the bytes read (K and V at one byte per element, their scales,
+    Q, O and LSE)."""
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_fwd_splitkv_e4m3, fa_quantize_e4m3, fa_sync_status
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+
+    w = WORKLOADS[DECODE]
+    qc, kc, vc = make_qkv(w)
+    q = qc[:, 0].contiguous().to(dev)
+    k8, kd = fa_quantize_e4m3(kc.to(dev))
+    v8, vd = fa_quantize_e4m3(vc.to(dev), per_head=True)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.b, w.hq), dtype=torch.float32, device=dev)
+    from tiled_exact_attention_gb300 import _lib
+    from tiled_exact_attention_gb300.api import make_splitkv_e4m3_args
+    import ctypes
+
+    a = make_splitkv_e4m3_args(q, k8, kd, v8, vd, o, lse)
+    ws = torch.empty(int(_lib.load().fa_splitkv_e4m3_workspace_size(ctypes.byref(a), 0)), dtype=torch.uint8,
+                     device=dev)
+    used = fa_fwd_splitkv_e4m3(q, k8, kd, v8, vd, workspace=ws, out=o, lse=lse, return_splits=True)[2]
+    ms = _timed(lambda: fa_fwd_splitkv_e4m3(q, k8, kd, v8, vd, workspace=ws, out=o, lse=lse), flush, steps, warmup)
+    if fa_sync_status() != 0:
+        raise RuntimeError("device status set by the e4m3 decode")
+    nbytes = (2 * w.b * w.skv * w.hkv * w.d + (kd.numel() + vd.numel()) * 4 + 2 * w.b * w.hq * w.d * 2
+              + w.b * w.hq * 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = float(_peaks()[0]["hbm_gbs"])
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4), "bytes_per_launch": nbytes,
+            "config": {"b": w.b, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "num_splits": used,
+                       "kv": "e4m3 codes, K scale per 128 keys, V scale per head"},
+            "keys_per_s": round(w.b * w.hkv * w.skv / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": _profiled_traffic("fa_decode_kernel_e4m3")},
+            "steps": steps}
 
 
 def _timed(step, flush, steps, warmup=3):

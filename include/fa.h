@@ -394,6 +394,45 @@ typedef struct {
 
 fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* args, void* stream);
 
+/*
+ * Split-KV decode over e4m3 keys and values ("hs-black: FlashAttention 1/2/3",
+ * section "FlashAttention-3: precision and hardware": a scale per block, carried
+ * into the computation; the split and its LSE-weighted merge of "ai-reference-codex:
+ * forward CUDA kernel", section 7).  One query row per (batch, query head), in
+ * bf16 / fp16, sees every one of the skv keys of its KV head (decode: the query
+ * stands at position skv - 1).  K as produced by fa_quantize_e4m3 (one scale per
+ * 128-key block), V by fa_quantize_e4m3 with per_head = 1 (not transposed):
+ *   s_j = (q . K8_j) * k_descale[block of j] * scale,  p_j = exp(s_j - m),
+ *   O = (sum_j p_j V8_j) * v_descale / sum_j p_j,  LSE = m + log sum_j p_j,
+ * with the scores, the probabilities and every sum in fp32 (K and V are widened
+ * exactly from e4m3; nothing is rounded to 8 bits on the way).  The key blocks
+ * are cut into num_splits ranges (0 = the split-count heuristic); the last CTA of
+ * each (batch, head group) merges the splits.  The workspace rules are those of
+ * fa_fwd_splitkv.  d in {64, 128}.
+ */
+typedef struct {
+  fa_dtype dtype;                 /* of q and o */
+  int32_t b, skv, hq, hkv, d;     /* hq % hkv == 0; skv >= 0 */
+  const void* q;                  /* device, [b, hq, d] of dtype */
+  int64_t q_strides[2];           /* (batch, head), in elements, multiples of 8 */
+  const void* k;                  /* device, e4m3 [b, skv, hkv, d] */
+  const void* v;                  /* device, e4m3 [b, skv, hkv, d] */
+  int64_t k_strides[3];           /* (batch, row, head), in bytes, multiples of 16 */
+  int64_t v_strides[3];
+  const float* k_descale;         /* device, [b, hkv, ceil(skv / 128)] */
+  const float* v_descale;         /* device, [b, hkv] */
+  void* o;                        /* device, [b, hq, d] of dtype, written */
+  int64_t o_strides[2];           /* (batch, head), in elements */
+  float* lse;                     /* device, fp32 [b, hq], written */
+  float scale;                    /* finite, > 0 */
+} fa_splitkv_e4m3_args;
+
+/* Workspace bytes fa_fwd_splitkv_e4m3 needs for num_splits splits (0 = its default); 0 if invalid. */
+size_t fa_splitkv_e4m3_workspace_size(const fa_splitkv_e4m3_args* args, int32_t num_splits);
+
+fa_status fa_fwd_splitkv_e4m3(const fa_splitkv_e4m3_args* args, int32_t num_splits, void* workspace,
+                              size_t workspace_bytes, int32_t* splits_used, void* stream);
+
 /* Size of the built-in split-KV scratch used by fa_fwd_splitkv_noalloc (per device). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

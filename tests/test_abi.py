@@ -108,6 +108,7 @@ int main(void) {
   printf("fa_bwd_args size %zu\n", sizeof(fa_bwd_args));
   printf("fa_quant_args size %zu\n", sizeof(fa_quant_args));
   printf("fa_fwd_e4m3_args size %zu\n", sizeof(fa_fwd_e4m3_args));
+  printf("fa_splitkv_e4m3_args size %zu\n", sizeof(fa_splitkv_e4m3_args));
   FIELDS
   return 0;
 }
@@ -117,14 +118,16 @@ int main(void) {
 def test_ctypes_mirrors_match_header_layout(tmp_path):
     """Every field of the ctypes mirrors sits at the offset, with the size, that a C
     compiler gives the structs declared in include/fa.h."""
-    from tiled_exact_attention_gb300._lib import BwdArgs, E4m3Args, FwdArgs, KvcacheArgs, QuantArgs, VarlenArgs
+    from tiled_exact_attention_gb300._lib import (BwdArgs, E4m3Args, FwdArgs, KvcacheArgs, QuantArgs, SplitkvE4m3Args,
+                                                  VarlenArgs)
 
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
     fields = []
     mirrors = {"fa_fwd_args": FwdArgs, "fa_kvcache_args": KvcacheArgs, "fa_varlen_args": VarlenArgs,
-               "fa_bwd_args": BwdArgs, "fa_quant_args": QuantArgs, "fa_fwd_e4m3_args": E4m3Args}
+               "fa_bwd_args": BwdArgs, "fa_quant_args": QuantArgs, "fa_fwd_e4m3_args": E4m3Args,
+               "fa_splitkv_e4m3_args": SplitkvE4m3Args}
     for cname, py in mirrors.items():
         for name, _ in py._fields_:
             fields.append(f"F({cname}, {name})")
@@ -316,3 +319,34 @@ def test_e4m3_validation(lib):
         setattr(a, field, value)
         assert lib.fa_fwd_e4m3(ctypes.byref(a), None) == expect, field
         setattr(a, field, old)
+
+
+def test_splitkv_e4m3_validation(lib):
+    from tiled_exact_attention_gb300._lib import SplitkvE4m3Args
+
+    def args(**kw):
+        a = SplitkvE4m3Args()
+        a.dtype, a.b, a.skv, a.hq, a.hkv, a.d = 0, 2, 256, 8, 2, 128
+        for f in ("q", "k", "v", "k_descale", "v_descale", "o", "lse"):
+            setattr(a, f, 4096)
+        a.q_strides = (ctypes.c_int64 * 2)(8 * 128, 128)
+        a.o_strides = (ctypes.c_int64 * 2)(8 * 128, 128)
+        a.k_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+        a.v_strides = (ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 128)
+        a.scale = 0.1
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    for field, value, expect in (("d", 96, 2), ("d", 256, 2), ("hq", 3, 1), ("q", 0, 1), ("k", 0, 1),
+                                 ("k_descale", 0, 1), ("scale", 0.0, 1), ("dtype", 5, 1), ("lse", 4098, 1)):
+        a = args(**{field: value})
+        assert lib.fa_fwd_splitkv_e4m3(ctypes.byref(a), 0, None, 0, None, None) == expect, field
+        assert lib.fa_splitkv_e4m3_workspace_size(ctypes.byref(a), 2) == 0, field
+    a = args(k_strides=(ctypes.c_int64 * 3)(256 * 2 * 128, 2 * 128, 8))  # not a multiple of 16 bytes
+    assert lib.fa_fwd_splitkv_e4m3(ctypes.byref(a), 0, None, 0, None, None) == 1
+    a = args()
+    # an explicit split count is sized without a device: two 128-key blocks cap 5 splits at 2
+    assert lib.fa_splitkv_e4m3_workspace_size(ctypes.byref(a), 5) == lib.fa_splitkv_e4m3_workspace_size(
+        ctypes.byref(a), 2) > 0
+    assert lib.fa_fwd_splitkv_e4m3(ctypes.byref(a), 2, None, 0, None, None) in (1, 3)  # no workspace / no device

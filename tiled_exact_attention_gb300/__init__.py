@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     fa_fwd_splitkv,
     fa_fwd_e4m3,
     fa_fwd_splitkv_noalloc,
+    fa_fwd_splitkv_e4m3,
     fa_fwd_varlen,
     fa_num_splits_heuristic,
     fa_quantize_e4m3,

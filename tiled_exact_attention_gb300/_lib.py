@@ -36,6 +36,8 @@ EXPORTS = (
     "fa_bwd_workspace_size",
     "fa_bwd",
     "fa_quantize_e4m3",
+    "fa_splitkv_e4m3_workspace_size",
+    "fa_fwd_splitkv_e4m3",
     "fa_fwd_e4m3",
     "fa_splitkv_combine",
     "fa_sync_status",
@@ -227,6 +229,31 @@ class E4m3Args(ctypes.Structure):
     ]
 
 
+class SplitkvE4m3Args(ctypes.Structure):
+    """Mirror of `fa_splitkv_e4m3_args`."""
+
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("b", ctypes.c_int32),
+        ("skv", ctypes.c_int32),
+        ("hq", ctypes.c_int32),
+        ("hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("q_strides", ctypes.c_int64 * 2),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("v_strides", ctypes.c_int64 * 3),
+        ("k_descale", ctypes.c_void_p),
+        ("v_descale", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("o_strides", ctypes.c_int64 * 2),
+        ("lse", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+    ]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -277,6 +304,11 @@ def load():
         lib.fa_quantize_e4m3.restype = ctypes.c_int
         lib.fa_fwd_e4m3.argtypes = [ctypes.POINTER(E4m3Args), vp]
         lib.fa_fwd_e4m3.restype = ctypes.c_int
+        pse = ctypes.POINTER(SplitkvE4m3Args)
+        lib.fa_splitkv_e4m3_workspace_size.argtypes = [pse, i32]
+        lib.fa_splitkv_e4m3_workspace_size.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv_e4m3.argtypes = [pse, i32, vp, ctypes.c_size_t, ctypes.POINTER(i32), vp]
+        lib.fa_fwd_splitkv_e4m3.restype = ctypes.c_int
         lib.fa_splitkv_combine.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp,
                                            ctypes.POINTER(i64), vp, vp]
         lib.fa_splitkv_combine.restype = ctypes.c_int

@@ -14,7 +14,7 @@ import torch
 
 from . import _lib
 from ._lib import (FA_BF16, FA_FP16, FA_OFFSET_BOTTOM_RIGHT, BwdArgs, E4m3Args, FwdArgs, KvcacheArgs, QuantArgs,
-                   VarlenArgs, check)
+                   SplitkvE4m3Args, VarlenArgs, check)
 
 _DT = {torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
 
@@ -395,6 +395,56 @@ def fa_fwd_e4m3(q8, q_descale, k8, k_descale, vt8, v_descale, *, causal: bool = 
         a.local = 1
         a.window_left, a.window_right = int(window[0]), int(window[1])
     check(_lib.load().fa_fwd_e4m3(ctypes.byref(a), _stream_handle(stream)), "fa_fwd_e4m3")
+    return out, lse
+
+
+def make_splitkv_e4m3_args(q, k8, k_descale, v8, v_descale, o, lse, *, scale=None) -> SplitkvE4m3Args:
+    """Fill `fa_splitkv_e4m3_args`: q, o [b, hq, d] bf16/fp16; k8, v8 e4m3 codes (torch.uint8) [b, skv, hkv, d];
+    k_descale [b, hkv, ceil(skv / 128)], v_descale [b, hkv] (fa_quantize_e4m3, V with per_head=True)."""
+    if not isinstance(q, torch.Tensor) or not q.is_cuda or q.dtype not in _DT or q.dim() != 3 or q.stride(2) != 1:
+        raise ValueError("q must be a CUDA bf16/fp16 [b, hq, d] tensor with contiguous d")
+    for name, t in (("k8", k8), ("v8", v8)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 \
+                or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a CUDA uint8 [b, skv, hkv, d] tensor with contiguous d")
+    b, hq, d = q.shape
+    skv, hkv = k8.shape[1], k8.shape[2]
+    if k8.shape != (b, skv, hkv, d) or v8.shape != k8.shape or o.shape != q.shape:
+        raise ValueError("inconsistent q / k8 / v8 / out shapes")
+    a = SplitkvE4m3Args()
+    a.dtype = _DT[q.dtype]
+    a.b, a.skv, a.hq, a.hkv, a.d = b, skv, hq, hkv, d
+    a.q = q.data_ptr()
+    a.q_strides = (ctypes.c_int64 * 2)(q.stride(0), q.stride(1))
+    a.k, a.v = k8.data_ptr(), v8.data_ptr()
+    a.k_strides = (ctypes.c_int64 * 3)(k8.stride(0), k8.stride(1), k8.stride(2))
+    a.v_strides = (ctypes.c_int64 * 3)(v8.stride(0), v8.stride(1), v8.stride(2))
+    a.k_descale, a.v_descale = k_descale.data_ptr(), v_descale.data_ptr()
+    a.o = o.data_ptr()
+    a.o_strides = (ctypes.c_int64 * 2)(o.stride(0), o.stride(1))
+    a.lse = lse.data_ptr()
+    a.scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    return a
+
+
+def fa_fwd_splitkv_e4m3(q, k8, k_descale, v8, v_descale, *, scale=None, num_splits: int = 0, workspace=None,
+                        out=None, lse=None, stream=None, return_splits=False):
+    """Decode one query row per (batch, head) against e4m3 keys and values; returns (O [b, hq, d], LSE [b, hq])."""
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    a = make_splitkv_e4m3_args(q, k8, k_descale, v8, v_descale, out, lse, scale=scale)
+    lib = _lib.load()
+    if workspace is None:
+        need = int(lib.fa_splitkv_e4m3_workspace_size(ctypes.byref(a), int(num_splits)))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    used = ctypes.c_int32(0)
+    check(lib.fa_fwd_splitkv_e4m3(ctypes.byref(a), int(num_splits), ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel() * workspace.element_size(), ctypes.byref(used),
+                                  _stream_handle(stream)), "fa_fwd_splitkv_e4m3")
+    if return_splits:
+        return out, lse, int(used.value)
     return out, lse
 
 

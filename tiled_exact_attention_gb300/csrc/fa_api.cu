@@ -142,9 +142,10 @@ bool encode_map(CUtensorMap* m, const void* ptr, fa_dtype dt, int d, int h, int 
 
 // General 4-D map over one-byte elements: dims innermost first, strides in bytes
 // of dims 1..3, the given box, 128-byte swizzle.
-// Box rows of box_in[0] bytes: the 128-byte swizzle, or the 64-byte one for 64-byte rows.
+// Box rows of box_in[0] bytes: the 128-byte swizzle, or the 64-byte one for 64-byte
+// rows; swizzle = false: plain row-major boxes (the CUDA-core decode reads them so).
 bool encode_map_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], const int64_t strides_b[3],
-                   const uint32_t box_in[4]) {
+                   const uint32_t box_in[4], bool swizzle = true) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[4];
@@ -153,7 +154,9 @@ bool encode_map_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], c
                            static_cast<cuuint64_t>(strides_b[2])};
   cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  const CUtensorMapSwizzle sw = box_in[0] == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle sw = !swizzle          ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                : box_in[0] == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_128B;
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1177,6 +1180,124 @@ fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* a, void* stream) {
   p.v_descale = a->v_descale;
   p.n_kblocks = static_cast<int>(ceil_div64(a->skv, 128));
   return from_cuda(launch_prefill_e4m3(p, a->d, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+fa_status validate_splitkv_e4m3(const fa_splitkv_e4m3_args* a) {
+  if (a == nullptr) return FA_ERR_INVALID_ARG;
+  if (a->dtype != FA_BF16 && a->dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (a->b < 1 || a->skv < 0 || a->hq < 1 || a->hkv < 1 || a->hq % a->hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale)) return FA_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128) return FA_ERR_UNSUPPORTED;
+  if (a->skv > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (a->q == nullptr || a->o == nullptr || a->lse == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->o, 16) || !aligned(a->lse, 4)) return FA_ERR_INVALID_ARG;
+  for (int i = 0; i < 2; ++i)
+    if (a->q_strides[i] <= 0 || a->q_strides[i] % 8 != 0 || a->o_strides[i] <= 0 || a->o_strides[i] % 8 != 0)
+      return FA_ERR_INVALID_ARG;
+  if (a->skv > 0) {
+    if (a->k == nullptr || a->v == nullptr || a->k_descale == nullptr || a->v_descale == nullptr)
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->k_descale, 4) || !aligned(a->v_descale, 4))
+      return FA_ERR_INVALID_ARG;
+    if (!strides16_ok(a->k_strides) || !strides16_ok(a->v_strides)) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+// Split count of the e4m3 decode: the heuristic over its CTAs (a group of up to 4
+// query heads of one KV head each) and resident slots, or the request, capped at
+// the key blocks there are.
+int splitkv_e4m3_splits(const fa_splitkv_e4m3_args* a, int32_t requested, const DeviceInfo* di) {
+  const int bn = decode_e4m3_block_n();
+  const int64_t nblk = ceil_div64(a->skv, bn);
+  int64_t ns = requested;
+  if (ns <= 0) {
+    if (di == nullptr) return 1;
+    const int g = a->hq / a->hkv;
+    const int64_t units = static_cast<int64_t>(a->b) * a->hkv * (g / decode_heads_per_cta(g));
+    ns = fa_num_splits_heuristic(units, di->sms, nblk, kMaxSplits);
+  }
+  const int64_t cap = nblk > 0 ? nblk : 1;
+  if (ns > cap) ns = cap;
+  if (ns > kMaxSplits * 8) ns = kMaxSplits * 8;
+  return ns < 1 ? 1 : static_cast<int>(ns);
+}
+
+size_t splitkv_e4m3_ws_bytes(const fa_splitkv_e4m3_args* a, int ns) {
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
+  return align256(rows * a->d * sizeof(float)) + align256(rows * sizeof(float)) + counters_bytes(a->b, a->hq);
+}
+
+}  // namespace
+
+size_t fa_splitkv_e4m3_workspace_size(const fa_splitkv_e4m3_args* a, int32_t num_splits) {
+  if (validate_splitkv_e4m3(a) != FA_OK || num_splits < 0) return 0;
+  if (num_splits > 0) return splitkv_e4m3_ws_bytes(a, splitkv_e4m3_splits(a, num_splits, nullptr));
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  return splitkv_e4m3_ws_bytes(a, splitkv_e4m3_splits(a, 0, &di));
+}
+
+fa_status fa_fwd_splitkv_e4m3(const fa_splitkv_e4m3_args* a, int32_t num_splits, void* workspace,
+                              size_t workspace_bytes, int32_t* splits_used, void* stream) {
+  const fa_status v = validate_splitkv_e4m3(a);
+  if (v != FA_OK) return v;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return FA_ERR_CUDA;
+  const int ns = splitkv_e4m3_splits(a, num_splits, &di);
+  const size_t need = splitkv_e4m3_ws_bytes(a, ns);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(ns) * a->b * a->hq;
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int bn = decode_e4m3_block_n();
+  if (a->skv > 0) {
+    // (d, hkv, rows, batch) views of K and V, one plain box of bn rows of d bytes
+    const uint64_t dims[4] = {static_cast<uint64_t>(a->d), static_cast<uint64_t>(a->hkv),
+                              static_cast<uint64_t>(a->skv), static_cast<uint64_t>(a->b)};
+    const int64_t ks[3] = {a->k_strides[2], a->k_strides[1], a->k_strides[0]};
+    const int64_t vs[3] = {a->v_strides[2], a->v_strides[1], a->v_strides[0]};
+    const uint32_t box[4] = {static_cast<uint32_t>(a->d), 1, static_cast<uint32_t>(bn), 1};
+    if (!encode_map_u8(&p.tm_k, a->k, dims, ks, box, false) || !encode_map_u8(&p.tm_v, a->v, dims, vs, box, false))
+      return FA_ERR_INVALID_ARG;
+  }
+  p.q = a->q;
+  p.q_stride_b = a->q_strides[0];
+  p.q_stride_h = a->q_strides[1];
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * a->d * sizeof(float)));
+  p.b = a->b;
+  p.skv = a->skv;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.g = a->hq / a->hkv;
+  p.kv_limit = a->skv;
+  p.kv_start = 0;
+  p.window_left = -1;
+  p.nblk = static_cast<int>(ceil_div64(a->skv, bn));
+  p.num_splits = ns;
+  p.blocks_per_split = static_cast<int>(ceil_div64(p.nblk > 0 ? p.nblk : 1, ns));
+  p.scale_log2 = static_cast<float>(static_cast<double>(a->scale) * 1.4426950408889634);
+  p.status = di.status;
+  p.kv_mode = kKvDense;
+  p.box_rows = bn;
+  p.counters = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(p.lse_part) + align256(rows * sizeof(float)));
+  p.o = a->o;
+  p.o_stride_b = a->o_strides[0];
+  p.o_stride_h = a->o_strides[1];
+  p.lse = a->lse;
+  p.k_descale = a->k_descale;
+  p.v_descale = a->v_descale;
+  p.n_kblocks = p.nblk;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(p.counters, 0, counters_bytes(a->b, a->hq), st);
+  if (e == cudaSuccess) e = launch_decode_e4m3(p, a->d, a->dtype, st);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (splits_used) *splits_used = ns;
+  return FA_OK;
 }
 
 fa_status fa_sync_status(void* stream) {

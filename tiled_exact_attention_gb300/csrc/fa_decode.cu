@@ -32,15 +32,18 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kDecWarps = 8;        // compute warps
 constexpr int kDecSubRows = 64;     // rows of the smallest TMA box (a 64-key page)
 
-template <int D>
+// E8: e4m3 K and V (one byte per element), 128-key blocks so that each block has
+// one K scale (the quantiser's 128-row blocks).
+template <int D, bool E8 = false>
 struct DecCfg {
+  static constexpr int ELT = E8 ? 1 : 2;  // bytes per K / V element
   // keys per ring stage: the larger the TMA boxes, the closer the stream gets to
   // the copy bandwidth (128-key stages measured 10% faster than 64-key ones at
   // d = 128); d = 256 keeps 64 so that three stages still fit
-  static constexpr int BN = (D == 256) ? 64 : 128;
-  static constexpr int STAGES = (D == 256) ? 3 : (D == 128) ? 3 : 6;
+  static constexpr int BN = (D == 256 && !E8) ? 64 : 128;
+  static constexpr int STAGES = E8 ? ((D == 128) ? 6 : 12) : (D == 256) ? 3 : (D == 128) ? 3 : 6;
   static constexpr int ROWS_PER_WARP = BN / kDecWarps;
-  static constexpr int KV_BYTES = BN * D * 2;            // one K or V block
+  static constexpr int KV_BYTES = BN * D * ELT;          // one K or V block
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   // two compute warpgroups + one control warpgroup (producer and three idle
   // warps) so that registers can move to the compute warps: launched at 168 per
@@ -52,14 +55,15 @@ struct DecCfg {
   static constexpr int REG_CONTROL = 40;
 };
 
-template <int D, int G>
+template <int D, int G, bool E8 = false>
 struct DecLane {
   static_assert(G == 1 || G == 2 || G == 4, "heads per CTA");
   static constexpr int DPL = 16;                  // head dims per lane
-  static constexpr int SEG = DPL / 8;             // 16-byte segments per lane
+  static constexpr int ESEG = E8 ? 16 : 8;        // elements per 16-byte segment
+  static constexpr int SEG = DPL / ESEG;          // 16-byte segments per lane
   static constexpr int LPR = D / DPL;             // lanes per key row
   static constexpr int RPP = 32 / LPR;            // key rows per pass
-  static constexpr int PASSES = DecCfg<D>::ROWS_PER_WARP / RPP;
+  static constexpr int PASSES = DecCfg<D, E8>::ROWS_PER_WARP / RPP;
   static_assert(LPR <= 32 && 32 % LPR == 0, "lane layout");
   static_assert(PASSES >= 1, "rows per warp");
 };
@@ -80,6 +84,24 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   }
 }
 
+// Sixteen e4m3 values (element 0 in the lowest byte) to fp32, exactly: each byte
+// pair widens to an f16 pair (every e4m3 value is an f16 value), then to fp32.
+__device__ __forceinline__ void unpack16_e4m3(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint16_t pr = static_cast<uint16_t>(w[i] >> (16 * j));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
+      const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      f[4 * i + 2 * j] = x.x;
+      f[4 * i + 2 * j + 1] = x.y;
+    }
+  }
+}
+
 template <bool BF16>
 __device__ __forceinline__ float load_elem(const void* base, int64_t idx) {
   const uint16_t u = static_cast<const uint16_t*>(base)[idx];
@@ -92,17 +114,17 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t idx) {
 
 enum : int { kSiteDecEmpty = 16, kSiteDecFull, kSiteDecDrain };
 
-template <int D, int G, bool BF16, bool SC>
+template <int D, int G, bool BF16, bool SC, bool E8>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit);
 
 // Dynamic shared memory: the K/V ring, its barriers, the cross-warp merge buffer
 // [warps][G][D + 2] and two flag words (abort, merging CTA).
-template <int D, int G>
+template <int D, int G, bool E8 = false>
 constexpr int dec_smem_bytes() {
-  return DecCfg<D>::STAGES * DecCfg<D>::STAGE_BYTES + 2 * DecCfg<D>::STAGES * 8 + kDecWarps * G * (D + 2) * 4 + 16 +
-         128;
+  return DecCfg<D, E8>::STAGES * DecCfg<D, E8>::STAGE_BYTES + 2 * DecCfg<D, E8>::STAGES * 8 +
+         kDecWarps * G * (D + 2) * 4 + 16 + 128;
 }
 
 // SC: softcap, each score capped to c tanh(s / c) before the mask.
@@ -114,10 +136,10 @@ __device__ __forceinline__ int cache_seq_len(const DecodeParams& p, int k) {
 
 // CACHE: a paged or packed KV cache (p.kv_mode), a separate instantiation so that
 // the dense kernel keeps its code.
-template <int D, int G, bool BF16, bool SC, bool CACHE>
-__global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecCfg<D>;
-  using L = DecLane<D, G>;
+template <int D, int G, bool BF16, bool SC, bool CACHE, bool E8 = false>
+__global__ void __launch_bounds__(DecCfg<D, E8>::THREADS, 1) fa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecCfg<D, E8>;
+  using L = DecLane<D, G, E8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -249,7 +271,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
               c_row = row_base + r;
               c_outer = 0;
             }
-            const int off = j * p.box_rows * D * 2;
+            const int off = j * p.box_rows * D * C::ELT;
             tma_load_4d_hint(st + off, &p.tm_k, &full[slot], 0, kvh, c_row, c_outer, pol);
             tma_load_4d_hint(st + C::KV_BYTES + off, &p.tm_v, &full[slot], 0, kvh, c_row, c_outer, pol);
           }
@@ -265,7 +287,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1) fa_decode_kernel(const 
     // ------------------------------ compute warps ------------------------------
     // (each register budget covers only its own role's code)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_COMPUTE));
-    compute_split<D, G, BF16, SC>(p, smem, full, empty, red, flags, warp, lane, split, bi, kvh, h_first, blk_lo, nb,
+    compute_split<D, G, BF16, SC, E8>(p, smem, full, empty, red, flags, warp, lane, split, bi, kvh, h_first, blk_lo, nb,
                                   start, limit);
   }
 }
@@ -322,12 +344,16 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, float* wts, 
   }
 }
 
-template <int D, int G, bool BF16, bool SC>
+template <int D, int G, bool BF16, bool SC, bool E8>
 __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                               float* red, int* flags, int warp, int lane, int split, int bi, int kvh,
                                               int h_first, int blk_lo, int nb, int start, int limit) {
-  using C = DecCfg<D>;
-  using L = DecLane<D, G>;
+  using C = DecCfg<D, E8>;
+  using L = DecLane<D, G, E8>;
+  constexpr int ELT = C::ELT;
+  // e4m3: the K scales of this KV head's 128-key blocks (one block per stage) and
+  // its V scale, applied to the partial output
+  const float* kdsc = E8 ? p.k_descale + (static_cast<int64_t>(bi) * p.hkv + kvh) * p.n_kblocks : nullptr;
   const int c = lane % L::LPR;      // dim group of this lane
   const int rg = lane / L::LPR;     // row within a pass
   // dims owned: segment s covers [s * D / SEG + 8 c, + 8)
@@ -341,9 +367,9 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
 #pragma unroll
     for (int s = 0; s < L::SEG; ++s)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        q[h][8 * s + e] = load_elem<BF16>(qrow, s * (D / L::SEG) + 8 * c + e) * p.scale_log2;
-        acc[h][8 * s + e] = 0.f;
+      for (int e = 0; e < L::ESEG; ++e) {
+        q[h][L::ESEG * s + e] = load_elem<BF16>(qrow, s * (D / L::SEG) + L::ESEG * c + e) * p.scale_log2;
+        acc[h][L::ESEG * s + e] = 0.f;
       }
     m[h] = -INFINITY;
     l[h] = 0.f;
@@ -375,12 +401,14 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
         if (key >= limit || key < start) {
 #pragma unroll
           for (int sg = 0; sg < L::SEG; ++sg)
-            *reinterpret_cast<uint4*>(vw + kr * (D * 2) + 2 * (sg * (D / L::SEG) + 8 * c)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vw + kr * (D * ELT) + ELT * (sg * (D / L::SEG) + L::ESEG * c)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
       }
       __syncwarp();
     }
     // scores (log2 domain, scale folded into q) for this lane's row in each pass
+    const float kdb = E8 ? kdsc[blk_lo + i] : 1.f;  // (e4m3: this block's K scale)
     float sc[L::PASSES][G];
 #pragma unroll
     for (int ps = 0; ps < L::PASSES; ++ps) {
@@ -388,8 +416,11 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
       float kf[L::DPL];
 #pragma unroll
       for (int s = 0; s < L::SEG; ++s) {
-        const uint4 u = *reinterpret_cast<const uint4*>(ks + kr * (D * 2) + 2 * (s * (D / L::SEG) + 8 * c));
-        unpack8<BF16>(u, kf + 8 * s);
+        const uint4 u = *reinterpret_cast<const uint4*>(ks + kr * (D * ELT) + ELT * (s * (D / L::SEG) + L::ESEG * c));
+        if constexpr (E8)
+          unpack16_e4m3(u, kf);
+        else
+          unpack8<BF16>(u, kf + 8 * s);
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -403,6 +434,10 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
       for (int x = 1; x < L::LPR; x <<= 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[ps][h] += __shfl_xor_sync(0xffffffffu, sc[ps][h], x);
+      if constexpr (E8) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[ps][h] *= kdb;
+      }
       if constexpr (SC) {
         // capped scores (log2 units): c log2(e) tanh(s / c), before the mask
 #pragma unroll
@@ -447,8 +482,11 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
       float vf[L::DPL];
 #pragma unroll
       for (int s = 0; s < L::SEG; ++s) {
-        const uint4 u = *reinterpret_cast<const uint4*>(vs + kr * (D * 2) + 2 * (s * (D / L::SEG) + 8 * c));
-        unpack8<BF16>(u, vf + 8 * s);
+        const uint4 u = *reinterpret_cast<const uint4*>(vs + kr * (D * ELT) + ELT * (s * (D / L::SEG) + L::ESEG * c));
+        if constexpr (E8)
+          unpack16_e4m3(u, vf);
+        else
+          unpack8<BF16>(u, vf + 8 * s);
       }
 
 #pragma unroll
@@ -490,7 +528,8 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
 #pragma unroll
       for (int s = 0; s < L::SEG; ++s)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) my[h * (D + 2) + s * (D / L::SEG) + 8 * c + e] = acc[h][8 * s + e];
+        for (int e = 0; e < L::ESEG; ++e)
+          my[h * (D + 2) + s * (D / L::SEG) + L::ESEG * c + e] = acc[h][L::ESEG * s + e];
       if (c == 0) {
         my[h * (D + 2) + D] = m[h];
         my[h * (D + 2) + D + 1] = l[h];
@@ -518,7 +557,8 @@ __device__ __forceinline__ void compute_split(const DecodeParams& p, uint8_t* sm
     }
     const int hq = h_first + h;
     const int64_t prow = (static_cast<int64_t>(split) * p.b + bi) * p.hq + hq;  // sq == 1
-    p.o_part[prow * D + e] = Lsum > 0.f ? o / Lsum : 0.f;
+    const float vsc = E8 ? p.v_descale[static_cast<int64_t>(bi) * p.hkv + kvh] : 1.f;
+    p.o_part[prow * D + e] = Lsum > 0.f ? o / Lsum * vsc : 0.f;
     if (e == 0) p.lse_part[prow] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
   }
   // ---- fused merge: the last CTA of this (batch, group) to count itself in ----
@@ -543,6 +583,18 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t stream) {
   if (p.kv_mode != kKvDense)
     kern = sc ? fa_decode_kernel<D, G, BF16, true, true> : fa_decode_kernel<D, G, BF16, false, true>;
   const int smem = dec_smem_bytes<D, G>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_splits, p.hkv * (p.g / G), p.b);
+  kern<<<grid, C::THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int G, bool BF16>
+cudaError_t launch_dec_e4m3(const DecodeParams& p, cudaStream_t stream) {
+  using C = DecCfg<D, true>;
+  auto kern = fa_decode_kernel<D, G, BF16, false, false, true>;
+  const int smem = dec_smem_bytes<D, G, true>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.hkv * (p.g / G), p.b);
@@ -677,6 +729,26 @@ int decode_ctas_per_sm(int d, int dtype) {
   }
   if (cacheable) cache[dev][di][bf16 ? 1 : 0].store(n, std::memory_order_relaxed);
   return n;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_dec_e4m3_g(const DecodeParams& p, cudaStream_t stream) {
+  switch (decode_heads_per_cta(p.g)) {
+    case 1: return launch_dec_e4m3<D, 1, BF16>(p, stream);
+    case 2: return launch_dec_e4m3<D, 2, BF16>(p, stream);
+    default: return launch_dec_e4m3<D, 4, BF16>(p, stream);
+  }
+}
+
+int decode_e4m3_block_n() { return DecCfg<128, true>::BN; }
+
+cudaError_t launch_decode_e4m3(const DecodeParams& p, int d, int dtype, cudaStream_t stream) {
+  const bool bf16 = dtype == 0;
+  switch (d) {
+    case 64: return bf16 ? launch_dec_e4m3_g<64, true>(p, stream) : launch_dec_e4m3_g<64, false>(p, stream);
+    case 128: return bf16 ? launch_dec_e4m3_g<128, true>(p, stream) : launch_dec_e4m3_g<128, false>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int dtype, cudaStream_t stream) {

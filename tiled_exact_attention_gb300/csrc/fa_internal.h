@@ -100,6 +100,10 @@ struct DecodeParams {
   // Softcap (sc_b > 0): the score x (q.k * scale * log2 e) becomes sc_b * tanh(x / sc_b),
   // tanh through 2^(sc_k x) with sc_k = 2 / c; sc_b = c log2(e).
   float sc_k, sc_b;
+  // e4m3 K / V: per-128-key-block K scales [b][hkv][n_kblocks], per-head V scales [b][hkv]
+  const float* k_descale;
+  const float* v_descale;
+  int n_kblocks;
 };
 
 // Parameters of the backward kernels (recompute form: D and log2-scaled LSE per
@@ -158,6 +162,8 @@ int prefill_block_n(int d);   // keys per KV block of the prefill kernel
 int prefill_q_tiles(int d);   // 128-row Q tiles per CTA
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int dtype, cudaStream_t stream);
+cudaError_t launch_decode_e4m3(const DecodeParams& p, int d, int dtype, cudaStream_t stream);  // d in {64, 128}
+int decode_e4m3_block_n();  // keys per block of the e4m3 decode (one K scale per block)
 int decode_block_n(int d);
 int decode_ctas_per_sm(int d, int dtype);
 int decode_heads_per_cta(int g);  // query heads of one KV group handled by one CTA
