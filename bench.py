@@ -424,12 +424,13 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": {"value": round(job_throughput(flops, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "copy_only_ms": link["ms_per_step"],
-                "frac_of_copy_bound": round(link["ms_per_step"] / e2e_ms, 4),
+                "copy_in_bound_ms": link["h2d_only_ms"],
+                "frac_of_copy_bound": round(link["h2d_only_ms"] / e2e_ms, 4),
                 "link": link,
                 "what": "prefill through fa_fwd with pinned host Q/K/V copied in and O/LSE copied out each step; "
                         "pipelined over two buffer sets (step i + 1 copies in while step i computes and copies out); "
-                        "copy_only_ms = the same copies with no computation (the link's own time per step)"},
+                        "copy_in_bound_ms = the step's inputs copied in alone, no computation: no step can be "
+                        "shorter; frac_of_copy_bound = that over ms_per_step"},
         "gpu_launches": K * 2,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -468,12 +469,12 @@ def bench_config(dev, flush, w, steps=30, warmup=3):
     flops = 4.0 * w.d * w.visible_pairs_per_head() * w.b * w.hq
     tf = flops / (ms * 1e-3) / 1e12
     dt = "bf16" if w.dtype == "bf16" else "fp16"
-    kname = "fa_prefill_kernel" if w.d == 128 else f"fa_prefill_kernel_d{w.d}"
+    kname = {"gqa_long": "fa_prefill_kernel_gqa"}.get(w.name, f"fa_prefill_kernel_d{w.d}")
     return {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "flops_per_launch": flops,
             "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "dtype": dt,
                        "std": w.std, "causal": w.causal},
             "roofline": _tensor_roofline(tf, kernel=f"fa_prefill_kernel<{w.d}, {dt}>",
-                                         traffic=_profiled_traffic(kname) if w.d != 128 else None,
+                                         traffic=_profiled_traffic(kname),
                                          dtype_note=" (fp16 runs at the bf16 rate)" if dt == "fp16" else ""),
             "steps": steps}
 
@@ -523,11 +524,11 @@ def bench_link(qc, kc, vc, wp, stream, steps):
     ms = timed()
     ms_in = timed(do_out=False)
     ms_out = timed(do_in=False)
-    return {"ms_per_step": round(ms, 4), "h2d_gbs": round(h2d / (ms_in * 1e-3) / 1e9, 1),
-            "d2h_gbs": round(d2h / (ms_out * 1e-3) / 1e9, 1),
+    return {"ms_per_step": round(ms, 4), "h2d_only_ms": round(ms_in, 4), "d2h_only_ms": round(ms_out, 4),
+            "h2d_gbs": round(h2d / (ms_in * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (ms_out * 1e-3) / 1e9, 1),
             "both_gbs": round((h2d + d2h) / (ms * 1e-3) / 1e9, 1),
             "what": "cudaMemcpyAsync from / to pinned host buffers (torch copy_), three copy-in streams and one "
-                    "copy-out stream side by side"}
+                    "copy-out stream; ms_per_step with both directions at once, h2d_only_ms / d2h_only_ms each alone"}
 
 
 def bench_backward(dev, flush, steps=30, warmup=3):
@@ -683,7 +684,8 @@ def bench_variants(dev, flush, steps=20):
       * softcap: the causal prefill workload with every score capped to 30 tanh(s / 30);
       * varlen: 16 packed causal sequences, lengths drawn (seeded) from [256, 4096], H = 16, d = 128;
       * decode_g8: split-KV decode with 8 query heads per KV head (B = 8, Hq = 64, Hkv = 8, KV = 32768,
-        d = 128), whose heads are the rows of one tensor-core tile; KV GB/s against the measured copy peak.
+        d = 128), whose heads are the rows of one tensor-core tile; KV GB/s against the measured copy peak;
+      * decode_b1 / decode_d64: the split-KV decode at B = 1, and at d = 64.
     The tensor-core lines divide by the burst bf16 peak."""
     import numpy as np
     import torch
@@ -749,6 +751,26 @@ def bench_variants(dev, flush, steps=20):
                                    "kernels": "fa_prefill_kernel (heads as rows) + fa_combine_kernel"},
                         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                                      "frac": round(gbs / hbm, 4), "traffic": None}}
+    # split-KV decode at a small batch (B = 1, the decode workload otherwise) and at d = 64 (B = 8, Hq = 32,
+    # Hkv = 8, KV = 32768): KV GB/s against the measured copy peak
+    for key, (b, hq, hkv, d) in (("decode_b1", (1, 32, 8, 128)), ("decode_d64", (8, 32, 8, 64))):
+        skv = 32768
+        qd, kd, vd = (t.to(dev) for t in make_custom(b, 1, skv, hq, hkv, d, "bf16", seed=BASE_SEED + 80))
+        od = torch.empty_like(qd)
+        ld = torch.empty((b, hq, 1), dtype=torch.float32, device=dev)
+        work = torch.empty(fa_splitkv_workspace_size(qd, kd, vd, 0, causal=True, q_pos_offset=skv - 1),
+                           dtype=torch.uint8, device=dev)
+        used = fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od, lse=ld,
+                              return_splits=True)[2]
+        ms = _timed(lambda: fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od,
+                                           lse=ld), flush, steps)
+        nbytes = 2 * b * skv * hkv * d * 2 + 2 * b * hq * d * 2 + b * hq * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[key] = {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                    "config": {"b": b, "skv": skv, "hq": hq, "hkv": hkv, "d": d, "num_splits": used},
+                    "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                                 "frac": round(gbs / hbm, 4), "traffic": None}}
+        del qd, kd, vd, work
     if fa_sync_status() != 0:
         raise RuntimeError("device status set by a forward-pass variant")
     return out
@@ -902,8 +924,9 @@ def _pairs(w, rows):
 
 
 def cpu_baseline(budget_s=15.0, seed=1):
-    """Time the oracle as it stands on the host cores over a random sample of the
-    prefill workload's rows; report the algorithmic TFLOP/s of that sample."""
+    """Time the oracle as it stands on the host cores on the prefill workload: the whole
+    problem when a calibration run says it takes at most twice the budget, else a random
+    sample of its rows sized for the budget; report the algorithmic TFLOP/s."""
     import numpy as np
 
     import oracle
@@ -912,20 +935,26 @@ def cpu_baseline(budget_s=15.0, seed=1):
     w = WORKLOADS[PREFILL]
     qc, kc, vc = make_qkv(w)
     q, k, v = (t.to(__import__("torch").float64).numpy() for t in (qc, kc, vc))
-    # calibrate on a small sample, then size the sample for the budget
+    total = w.b * w.hq * w.sq
+    # calibrate on a small sample, then take the whole problem or a sample sized for the budget
     rows = _sample_rows(w, 256, seed)
     t0 = time.perf_counter()
     oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
     t_small = max(time.perf_counter() - t0, 1e-3)
-    n = int(min(w.b * w.hq * w.sq, max(256, 256 * budget_s / t_small)))
-    rows = _sample_rows(w, n, seed + 1)
+    est_all = t_small * total / 256
+    if est_all <= 2 * budget_s:
+        rows = oracle.all_rows(w.b, w.hq, w.sq)
+        what = "the whole causal prefill workload (every row of every head and batch)"
+    else:
+        n = int(min(total, max(256, 256 * budget_s / t_small)))
+        rows = _sample_rows(w, n, seed + 1)
+        what = f"{n} random query rows of the causal prefill workload (all heads/batches)"
     t0 = time.perf_counter()
     oracle.attention(q, k, v, causal=True, q_pos_offset=w.offset, rows=rows)
     dt = time.perf_counter() - t0
     flops = 4.0 * w.d * _pairs(w, rows)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} random query rows of the causal prefill workload (all heads/batches), "
-                      f"{_pairs(w, rows)} visible pairs, {dt:.2f} s, fp64 C oracle with OpenMP",
+            "sample": f"{what}, {_pairs(w, rows)} visible pairs, {dt:.2f} s, fp64 C oracle with OpenMP",
             "seconds": round(dt, 3)}
 
 
