@@ -469,7 +469,7 @@ def bench_config(dev, flush, w, steps=30, warmup=3):
     flops = 4.0 * w.d * w.visible_pairs_per_head() * w.b * w.hq
     tf = flops / (ms * 1e-3) / 1e12
     dt = "bf16" if w.dtype == "bf16" else "fp16"
-    kname = {"gqa_long": "fa_prefill_kernel_gqa"}.get(w.name, f"fa_prefill_kernel_d{w.d}")
+    kname = {"gqa_long": "fa_prefill_kernel_gqa", "causal_prefill": "fa_prefill_kernel"}.get(w.name, f"fa_prefill_kernel_d{w.d}")
     return {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "flops_per_launch": flops,
             "config": {"b": w.b, "sq": w.sq, "skv": w.skv, "hq": w.hq, "hkv": w.hkv, "d": w.d, "dtype": dt,
                        "std": w.std, "causal": w.causal},
