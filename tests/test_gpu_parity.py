@@ -169,6 +169,28 @@ def test_output_only_16_byte_aligned(d):
     assert torch.all(pad == 3.0)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("dts", ["bf16", "fp16"])
+def test_output_with_gaps_between_heads_rows_and_batches(d, dts):
+    """O written into a larger buffer with gaps after every head, row and batch
+    (the tile stores address O through its strides; a 333-row sequence leaves
+    store tiles partly past its end): equal to the contiguous result, and no
+    element outside O is touched."""
+    b, s, h = 2, 333, 3
+    q, k, v = _cuda(*make_custom(b, s, s, h, h, d, dts, seed=81 + d))
+    o1, l1 = fa_fwd(q, k, v, causal=True)
+    sh, sr = d + 8, h * (d + 8) + 16
+    sb = s * sr + 64
+    buf = torch.full((b * sb,), 7.0, dtype=q.dtype, device=DEV)
+    o2 = buf.as_strided((b, s, h, d), (sb, sr, sh, 1))
+    fa_fwd(q, k, v, causal=True, out=o2)
+    assert fa_sync_status() == 0
+    assert torch.equal(o1, o2)
+    mask = torch.ones_like(buf, dtype=torch.bool)
+    mask.as_strided((b, s, h, d), (sb, sr, sh, 1)).fill_(False)
+    assert torch.all(buf[mask] == 7.0)
+
+
 def test_deterministic():
     q, k, v = _cuda(*make_custom(1, 640, 640, 4, 4, 128, "bf16", seed=5))
     o1, l1 = fa_fwd(q, k, v, causal=True)

@@ -529,6 +529,7 @@ fa_status fa_fwd(const fa_fwd_args* a, void* stream) {
   p.o_stride_h = a->o_strides[2];
   p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0 &&
               a->o_strides[2] % 16 == 0;
+  p.o_tma = encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->sq, a->b, a->o_strides, 64, 32, true) ? 1 : 0;
   p.b = a->b;
   p.sq = a->sq;
   p.skv = a->skv;
@@ -884,6 +885,10 @@ fa_status fa_fwd_varlen(const fa_varlen_args* a, void* stream) {
   p.o_stride_row = a->o_strides[0];
   p.o_stride_h = a->o_strides[1];
   p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0;
+  {
+    const auto os = st3(a->o_strides, a->total_q);
+    p.o_tma = encode_map(&p.tm_o, a->o, a->dtype, a->d, a->hq, a->total_q, 1, os.data(), 64, 32, true) ? 1 : 0;
+  }
   p.b = a->b;
   p.sq = a->max_seqlen_q;
   p.skv = 0;
@@ -1158,6 +1163,7 @@ fa_status fa_fwd_e4m3(const fa_fwd_e4m3_args* a, void* stream) {
   p.o_stride_h = a->o_strides[2];
   p.o_vec32 = aligned(a->o, 32) && a->o_strides[0] % 16 == 0 && a->o_strides[1] % 16 == 0 &&
               a->o_strides[2] % 16 == 0;
+  p.o_tma = encode_map(&p.tm_o, a->o, FA_BF16, a->d, a->hq, a->sq, a->b, a->o_strides, 64, 32, true) ? 1 : 0;
   p.b = a->b;
   p.sq = a->sq;
   p.skv = a->skv;

@@ -12,11 +12,16 @@ struct PrefillParams {
   CUtensorMap tm_q;  // Q  [b][sq][hq][d],  box {64, 1, 128, 1}
   CUtensorMap tm_k;  // K  [b][skv][hkv][d], box {64, 1, BN, 1}
   CUtensorMap tm_v;  // V  same as K
-  void* o;           // O base (written row by row by the softmax threads)
+  // O [b][sq][hq][d] (or [total_q][hq][d] as (d, hq, total_q, 1)), box {64, 1, 32, 1},
+  // 128-byte swizzle: each softmax warp stores its 32 rows from shared memory (valid
+  // when o_tma != 0)
+  CUtensorMap tm_o;
+  void* o;           // O base (written row by row by the softmax threads when o_tma == 0)
   float* lse;        // LSE [b][hq][sq] (or LSE partials [ns][b][hq][sq] in split mode)
   float* o_part;     // split mode: normalised partial outputs [ns][b][hq][sq][d]
   int64_t o_stride_b, o_stride_row, o_stride_h;  // elements
   int o_vec32;         // O rows may be written with 32-byte stores (base and strides 32-byte aligned)
+  int o_tma;           // tm_o maps O (16-bit outputs whose base and strides TMA accepts)
   int b, sq, skv, hq, hkv, g;
   int causal;          // right edge active: row i sees key j only if j <= i + off
   int off;
