@@ -67,7 +67,7 @@ struct Cfg {
   static constexpr int STG_OFF = RING_OFF + STAGES * KV_BYTES;
   static constexpr int STG_WARP = 32 * 128;
   static constexpr int BAR_OFF = STG_OFF + (TMA_O ? 4 * NQ * STG_WARP : 0);
-  static constexpr int NUM_BARS = 3 + 5 * NQ + 2 * STAGES;
+  static constexpr int NUM_BARS = 3 + 7 * NQ + 2 * STAGES;
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;
   // Register split (NQ == 2): launched at 168 per thread (384 threads), the
   // control warpgroup drops to 72 and the two softmax warpgroups rise to 216:
@@ -79,6 +79,13 @@ struct Cfg {
   static_assert(O_COL0 + NQ * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static __device__ __forceinline__ int s_col(int t) { return t * 128; }
+  // d = 256: P in TMEM columns of its own (S 64 + O 256 leave 192 free), so that
+  // the next block's S is computed while the softmax still works on this one
+  // (measured +17%).  d = 128 has no free columns (S 2 x 128 + O 2 x 128), and for
+  // d = 64, where 128 are free, the same measured 3-8% slower: there P
+  // overwrites S and the next S waits for the PV that reads it.
+  static constexpr bool P_SEP = D == 256;
+  static __device__ __forceinline__ int p_col(int t) { return P_SEP ? 128 : t * 128; }
   static __device__ __forceinline__ int o_col(int t) { return O_COL0 + t * D; }
 };
 
@@ -92,7 +99,9 @@ enum : int {
   kSiteOFull,
   kSiteDrain,
   kSiteQEmpty,
-  kSiteOEmpty
+  kSiteOEmpty,
+  kSiteSFree,
+  kSitePFree
 };
 
 // One work item: NQ Q tiles of one (split, batch or packed sequence, head) and
@@ -278,7 +287,9 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
   uint64_t* o_empty = o_full + NQ;
   uint64_t* mma_done = o_empty + NQ;
   uint64_t* p_half = mma_done + 1;  // P of the block's first half of keys written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + NQ);
+  uint64_t* s_free = p_half + NQ;   // (P_SEP) the softmax has loaded S: the next S may overwrite it
+  uint64_t* p_free = s_free + NQ;   // (P_SEP) a block's PV has completed: P may be rewritten, O rescaled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + NQ);
   uint8_t* ring = smem + C::RING_OFF;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -296,6 +307,8 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       mbar_init(&p_half[t], BM);
       mbar_init(&o_full[t], 1);
       mbar_init(&o_empty[t], BM);
+      mbar_init(&s_free[t], BM);
+      mbar_init(&p_free[t], 1);
     }
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) {
@@ -437,9 +450,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       // slot 0 read as V: MN-major (16-bit), or K-major V^T (e4m3)
       const uint64_t v_desc = E8 ? sdesc_sw128(ring_s, 16, 1024) : sdesc_sw128(ring_s, BN * 128, 1024);
       uint32_t gL = 0, q_uses = 0;
-      uint32_t pv_cnt[NQ], o_uses[NQ];
+      constexpr bool PS = C::P_SEP;
+      uint32_t pv_cnt[NQ], o_uses[NQ], s_iss[NQ];  // s_iss: S tiles issued per Q tile (P_SEP)
 #pragma unroll
-      for (int t = 0; t < NQ; ++t) pv_cnt[t] = o_uses[t] = 0;
+      for (int t = 0; t < NQ; ++t) pv_cnt[t] = o_uses[t] = s_iss[t] = 0;
       bool ok = true;
       for (int j = 0; ok; ++j) {
         const int item = item_of(j);
@@ -463,23 +477,52 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
 #pragma unroll
         for (int t = 0; t < NQ; ++t)
           if (FA_ACTIVE(t, 0)) {
+            if constexpr (PS) {  // the S buffer is free once the softmax has loaded the previous S
+              if (s_iss[t] > 0 && !issuer_wait<WI>(&s_free[t], (s_iss[t] - 1) & 1, p.status, kSiteSFree)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              ++s_iss[t];
+            }
             issue_s<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS, E8, WI>(tbase + C::s_col(t), q_desc, k_desc, t,
                                                                    gL % C::STAGES);
             umma_commit<WI>(&s_full[t]);
           }
+        if (!ok) break;
         if (N == 1) umma_commit<WI>(q_empty);  // the item's last S has been issued
         umma_commit<WI>(&kv_empty[gL % C::STAGES]);
         for (int it = 0; it < N; ++it) {
           const uint32_t Lv = gL + 2 * it + 1, Lk = gL + 2 * it + 2;
           const bool has_next = it + 1 < N;
+          bool k_ready = false;
           if (!issuer_wait<WI>(&kv_full[Lv % C::STAGES], (Lv / C::STAGES) & 1, p.status, kSiteKvFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          bool k_ready = false;
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
+            if (PS && has_next && FA_ACTIVE(t, it + 1)) {
+              // the tile's next S first: it waits only until the softmax has loaded
+              // the current S, and runs while the softmax forms P
+              if (!k_ready) {
+                if (!issuer_wait<WI>(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) {
+                  ok = false;
+                  break;
+                }
+                k_ready = true;
+              }
+              if (s_iss[t] > 0 && !issuer_wait<WI>(&s_free[t], (s_iss[t] - 1) & 1, p.status, kSiteSFree)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              ++s_iss[t];
+              issue_s<D, BN, BM, C::Q_BYTES, C::KV_BYTES, kIdS, E8, WI>(tbase + C::s_col(t), q_desc, k_desc, t,
+                                                                     Lk % C::STAGES);
+              umma_commit<WI>(&s_full[t]);
+            }
             if (FA_ACTIVE(t, it)) {
               if (!issuer_wait<WI>(HALF_P ? &p_half[t] : &p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
                 ok = false;
@@ -493,24 +536,25 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
               }
               tc_fence_after();
               if constexpr (!HALF_P) {
-                issue_pv<D, BN, C::KV_BYTES, kIdO, E8, WI>(tbase + C::o_col(t), tbase + C::s_col(t), v_desc,
+                issue_pv<D, BN, C::KV_BYTES, kIdO, E8, WI>(tbase + C::o_col(t), tbase + C::p_col(t), v_desc,
                                                            Lv % C::STAGES, !first);
               } else {
                 // the block's first 64 keys as soon as their P is written, then the rest
-                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 32, WI>(tbase + C::o_col(t), tbase + C::s_col(t),
+                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, 0, BN / 32, WI>(tbase + C::o_col(t), tbase + C::p_col(t),
                                                                        v_desc, Lv % C::STAGES, !first);
                 if (!issuer_wait<WI>(&p_full[t], pv_cnt[t] & 1, p.status, kSitePFull)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, BN / 32, BN / 16, WI>(tbase + C::o_col(t), tbase + C::s_col(t),
+                issue_pv_tile<D, BN, C::KV_BYTES, kIdO, BN / 32, BN / 16, WI>(tbase + C::o_col(t), tbase + C::p_col(t),
                                                                              v_desc, Lv % C::STAGES, true);
               }
+              if constexpr (PS) umma_commit<WI>(&p_free[t]);
               if (it + 1 == it_e[t]) umma_commit<WI>(&o_full[t]);  // the tile's last PV of the item
               ++pv_cnt[t];
             }
-            if (has_next && FA_ACTIVE(t, it + 1)) {
+            if (!PS && has_next && FA_ACTIVE(t, it + 1)) {
               if (!k_ready) {
                 if (!issuer_wait<WI>(&kv_full[Lk % C::STAGES], (Lk / C::STAGES) & 1, p.status, kSiteKvFull)) {
                   ok = false;
@@ -550,6 +594,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
     const int r = 32 * wq + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t tS = tbase + lane_off + C::s_col(t);
+    const uint32_t tP = tbase + lane_off + C::p_col(t);
     const uint32_t tO = tbase + lane_off + C::o_col(t);
     const float sl2 = p.scale_log2;
     const bool split_mode = p.o_part != nullptr;
@@ -626,7 +671,13 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         tc_fence_after();
         uint32_t sr[BN];
         tmem_load_row<BN>(tS, sr);
+        if constexpr (C::P_SEP) {  // the scores are in registers: the next S may overwrite them
+          tc_fence_before();
+          mbar_arrive(&s_free[t]);
+        }
         float* s = reinterpret_cast<float*>(sr);
+        // (P_SEP) P and O may be written once the previous block's PV has completed
+        bool pv_done = !C::P_SEP || gblk == 0;
         if constexpr (SC) {
           // capped scores in log2 units, c log2(e) tanh(s / c), before the mask sets -inf
 #pragma unroll
@@ -665,9 +716,18 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         float alpha = 1.f;  // (l_run is 0 before the first block: alpha is not needed there)
         if (k > 0 && __any_sync(0xffffffffu, grow)) {
+          if (!pv_done) {
+            if (!warp_wait(&p_free[t], (gblk - 1) & 1, p.status, kSitePFree)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv_done = true;
+          }
           alpha = grow ? ex2_approx(m_run - m_use) : 1.f;
-          // O_t already holds the previous blocks' product: S_k complete implies
-          // PV_{k-1} complete (one issuing thread, in-order completion).
+          // O_t holds the previous blocks' product: S_k complete implies PV_{k-1}
+          // complete when P overwrites S (one issuing thread, in-order completion),
+          // else the wait above.
           // 32 columns at a time: the 128 scores are still live in registers.
           constexpr int CH = 32;
 #pragma unroll
@@ -708,7 +768,16 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
               sum2[(c >> 2) & 3] = __fadd2_rn(sum2[(c >> 2) & 3], __fadd2_rn(e0, e1));
               pk[c >> 2] = pack4_e4m3(e0.x, e0.y, e1.x, e1.y);
             }
-            tmem_st16(tS + half * (BN / 8), pk);
+            if (!pv_done) {
+              if (!warp_wait(&p_free[t], (gblk - 1) & 1, p.status, kSitePFree)) break;
+              tc_fence_after();
+              pv_done = true;
+            }
+            tmem_st16(tP + half * (BN / 8), pk);
+          }
+          if (!pv_done) {
+            ok = false;
+            break;
           }
           tmem_st_wait();
           tc_fence_before();
@@ -734,14 +803,23 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
               add_packed_f16(sum2[(c >> 1) & 3], pk[c >> 1]);
             }
           }
+          if (!pv_done) {
+            if (!warp_wait(&p_free[t], (gblk - 1) & 1, p.status, kSitePFree)) break;
+            tc_fence_after();
+            pv_done = true;
+          }
 #pragma unroll
           for (int c = 0; c < BN / 4; c += 16)
-            tmem_st16(tS + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
+            tmem_st16(tP + half * (BN / 4) + c, *reinterpret_cast<const uint32_t(*)[16]>(pk + c));
           if (HALF_P || half == 1) {
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(half == 0 ? &p_half[t] : &p_full[t]);
           }
+        }
+        if (!pv_done) {
+          ok = false;
+          break;
         }
         }
         const float2 s01 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
