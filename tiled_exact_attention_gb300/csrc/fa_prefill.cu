@@ -42,6 +42,10 @@ struct Cfg {
   // keys per K/V block (e4m3: 128, so that a row of the transposed V tile is 128 bytes)
   static constexpr int BN = (D <= 128 || E8) ? 128 : 64;
   static constexpr int STAGES = E8 ? (D == 256 ? 4 : 8) : (D == 64 ? 8 : 4);  // K/V ring slots
+  // d = 256 (one row tile per CTA: every tile re-reads its head's K/V, mostly from
+  // DRAM) also prefetches each K/V block into L2 two blocks ahead of its load:
+  // measured +3.8% there, -3% on the causal d = 128 prefill
+  static constexpr int KV_PREFETCH = (D == 256 && !E8) ? 2 : 0;
   // Q and K rows are staged in swizzle chunks of CHUNK_BYTES: 128-byte rows with the
   // 128-byte swizzle, or (e4m3, d = 64) one 64-byte chunk with the 64-byte swizzle
   static constexpr int ROW_BYTES = D * ELT;
@@ -422,6 +426,15 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
             for (int c = 0; c < C::DC; ++c)
               tma_load_4d_hint(ring + slot * C::KV_BYTES + c * (BN * C::CHUNK_BYTES), map, &kv_full[slot], c * C::CHUNK_ELEMS,
                                w.kvh, w.k_base + n * BN, w.tbk, pol_kv);
+            if constexpr (C::KV_PREFETCH > 0) {
+              // warm L2 with the same tensor's block KV_PREFETCH blocks further on
+              const int npf = n - C::KV_PREFETCH;
+              if (npf >= w.n_hi_max - w.N) {
+#pragma unroll
+                for (int c = 0; c < C::DC; ++c)
+                  tma_prefetch_l2_4d(map, c * C::CHUNK_ELEMS, w.kvh, w.k_base + npf * BN, w.tbk);
+              }
+            }
           }
         }
       }
