@@ -19,7 +19,7 @@ rank's time.
 Every roofline divides by the measured burst bf16 GEMM peak (each launch lasts
 well under a millisecond, between L2 flushes); the sustained peak is reported
 beside it.  `--only NAME[,NAME...]` times just the named lines (prefill, decode,
-gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, paged, decode_e4m3, variants, e2e,
+gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, e4m3_d256, paged, decode_e4m3, variants, e2e,
 link)
 and prints them as one JSON object: the form the ncu captures use.
 """
@@ -205,7 +205,7 @@ def _setup(args):
     return ws, rank, dev, flush
 
 
-SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "decode_e4m3", "backward", "e4m3", "e4m3_d64",
+SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "decode_e4m3", "backward", "e4m3", "e4m3_d64", "e4m3_d256",
              "variants", "e2e", "link")
 
 
@@ -231,7 +231,7 @@ def run_only(args):
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup)
         elif nm == "decode_e4m3":
             out[nm] = bench_decode_e4m3(dev, flush, steps=steps, warmup=args.warmup)
-        elif nm == "e4m3_d64":
+        elif nm in ("e4m3_d64", "e4m3_d256"):
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup, workload="ragged_" + nm[5:])
         elif nm == "variants":
             out[nm] = bench_variants(dev, flush, steps=steps)
@@ -339,7 +339,7 @@ def run_ours(args):
     dec8 = bench_decode_e4m3(dev, flush, steps=max(20, min(500, K // 10)))
     bwd = bench_backward(dev, flush, steps=few)
     e4m3 = bench_e4m3(dev, flush, steps=max(10, min(200, K // 25)))
-    e4m3_rag = {f"e4m3_d{w}": bench_e4m3(dev, flush, steps=few, workload=f"ragged_d{w}") for w in (64,)}
+    e4m3_rag = {f"e4m3_d{w}": bench_e4m3(dev, flush, steps=few, workload=f"ragged_d{w}") for w in (64, 256)}
     variants = bench_variants(dev, flush, steps=few)
 
     flops = 4.0 * wp.d * wp.visible_pairs_per_head() * wp.b * wp.hq
@@ -417,6 +417,7 @@ def run_ours(args):
         "decode_e4m3": dec8,
         "e4m3": e4,
         "e4m3_d64": e4m3_rag["e4m3_d64"],
+        "e4m3_d256": e4m3_rag["e4m3_d256"],
         "backward": bw,
         "variants": variants,
         "roofline": dict(_tensor_roofline(per_gpu_tflops, kernel="fa_prefill_kernel<128, bf16>", traffic=pre_traffic),

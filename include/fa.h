@@ -362,7 +362,7 @@ typedef struct {
 fa_status fa_quantize_e4m3(const fa_quant_args* args, void* stream);
 
 /*
- * Forward pass with e4m3 Q, K, V (d in {64, 128}; FA_ERR_UNSUPPORTED otherwise): S = (Q8 K8^T) * q_descale[tile of
+ * Forward pass with e4m3 Q, K, V (d in {64, 128, 256}; FA_ERR_UNSUPPORTED otherwise): S = (Q8 K8^T) * q_descale[tile of
  * 128 rows] * k_descale[block of 128 keys] * scale, P = exp(S - m) rounded to e4m3
  * for the P V product (P <= 2^8 by the lazy-rescale rule, within e4m3's range),
  * row max and sum in fp32, O = (P8 V8) * v_descale[head] / l written as bf16,

@@ -313,7 +313,7 @@ def test_e4m3_validation(lib):
         setattr(a, f, (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128))
     a.o_strides = (ctypes.c_int64 * 3)(128 * 2 * 128, 2 * 128, 128)
     a.scale = 0.1
-    for field, value, expect in (("d", 96, 2), ("d", 256, 2), ("vt", 0, 1), ("v_descale", 0, 1), ("causal", 3, 1),
+    for field, value, expect in (("d", 96, 2), ("d", 512, 2), ("vt", 0, 1), ("v_descale", 0, 1), ("causal", 3, 1),
                                  ("scale", 0.0, 1), ("hq", 3, 1)):
         old = getattr(a, field)
         setattr(a, field, value)

@@ -123,9 +123,12 @@ struct ItemPlan {
   bool valid;                  // false: packed offsets out of range (nothing is touched)
 };
 
-template <int D, bool VARLEN, bool CACHE>
-__device__ __forceinline__ ItemPlan<Cfg<D>::NQ> plan_item(const PrefillParams& p, int item) {
-  using C = Cfg<D>;
+// E8 selects the 8-bit configuration, whose key blocks are 128 keys at every d
+// (the 16-bit d = 256 configuration uses 64): the plan counts blocks of the
+// kernel's own size.
+template <int D, bool VARLEN, bool CACHE, bool E8 = false>
+__device__ __forceinline__ ItemPlan<Cfg<D, E8>::NQ> plan_item(const PrefillParams& p, int item) {
+  using C = Cfg<D, E8>;
   constexpr int BM = C::BM, BN = C::BN, NQ = C::NQ;
   ItemPlan<NQ> w;
   // Items are numbered longest causal row-group first (longest-processing-time
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       for (int j = 0; ok; ++j) {
         const int item = item_of(j);
         if (item >= total_items) break;
-        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
+        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE, E8>(p, item);
         if (w.N == 0) continue;
         // Q buffer free: the previous item's S MMAs have completed
         if (q_loads > 0 && !mbar_wait(q_empty, (q_loads - 1) & 1, p.status, kSiteQEmpty)) break;
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
         if (item >= total_items) break;
         int N, it_b[NQ], it_e[NQ];  // tile t is active in iterations [it_b[t], it_e[t])
         {
-          const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
+          const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE, E8>(p, item);
           N = w.N;
 #pragma unroll
           for (int t = 0; t < NQ; ++t) {
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       float sl2q = sl2;        // e4m3: the tile's Q scale folded into the score scale
       const float* kd = nullptr;  // e4m3: the K scales of this head's key blocks
       {
-        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);
+        const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE, E8>(p, item);
         const uint32_t first_load = g_loads;
         if constexpr (CACHE) g_loads += 2 * w.N;
         if (VARLEN && !w.valid) {
@@ -842,7 +845,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1) fa_prefill_kernel(cons
       if (!ok) break;
 
       // ---------------- epilogue (overlaps the next item's first MMAs) ----------------
-      const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE>(p, item);  // recomputed: fewer registers in the loop
+      const ItemPlan<NQ> w = plan_item<D, VARLEN, CACHE, E8>(p, item);  // recomputed: fewer registers in the loop
       const bool valid = row < w.sq;
       // LSE [b][hq][sq], or [hq][total_q] for packed sequences
       const int64_t lse_idx = VARLEN ? static_cast<int64_t>(w.h) * p.total_q + w.q_base + row
@@ -1012,9 +1015,7 @@ cudaError_t launch_t(const PrefillParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// (d = 256 is not offered: its two-chunk 8-bit S product measured all zeros on the
-// GPU, a cause not found; the 16-bit path serves d = 256)
-bool prefill_e4m3_supported(int d) { return d == 64 || d == 128; }
+bool prefill_e4m3_supported(int d) { return d == 64 || d == 128 || d == 256; }
 
 template <int D>
 cudaError_t launch_e4m3_t(const PrefillParams& p, cudaStream_t stream) {
@@ -1035,6 +1036,7 @@ cudaError_t launch_prefill_e4m3(const PrefillParams& p, int d, cudaStream_t stre
   switch (d) {
     case 64: return launch_e4m3_t<64>(p, stream);
     case 128: return launch_e4m3_t<128>(p, stream);
+    case 256: return launch_e4m3_t<256>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
