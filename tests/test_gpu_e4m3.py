@@ -129,3 +129,48 @@ def test_e4m3_forward_matches_oracle_on_dequantised_inputs(case):
     if vmean:
         # the bound is tight enough to see a V scale applied twice (O doubled) or not at all
         assert np.mean(np.abs(o_ref[vis]) > tol[vis]) > 0.9
+
+
+def _draw_e4m3(i):
+    rng = np.random.default_rng(9100 + i)
+    d = int(rng.choice([64, 128, 256]))
+    g = int(rng.choice([1, 2, 4]))
+    hkv = int(rng.integers(1, 3))
+    b = int(rng.integers(1, 3))
+    sq = int(rng.integers(1, 600))
+    skv = int(rng.integers(1, 800))
+    causal = bool(rng.integers(0, 2))
+    off = int(rng.integers(-40, 500)) if causal and rng.integers(0, 2) else None
+    window = (int(rng.integers(-1, 250)), int(rng.integers(-1, 250))) if rng.integers(0, 3) == 0 else None
+    vmean = float(rng.choice([0.0, 0.0, 1.5, -2.0]))
+    return b, sq, skv, g * hkv, hkv, d, causal, off, window, vmean
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_e4m3_forward_random(i):
+    """Seeded random shapes (every head dimension, lengths cutting tiles anywhere,
+    groups, offsets, windows, shifted V) against the same per-element bound."""
+    b, sq, skv, hq, hkv, d, causal, off, window, vmean = case = _draw_e4m3(i)
+    q, k, v = make_custom(b, sq, skv, hq, hkv, d, "bf16", std=1.0, seed=9200 + i)
+    if vmean:
+        v = (v.float() + vmean).to(torch.bfloat16)
+    (q8, qd), (k8, kd), (vt8, vd) = (fa_quantize_e4m3(q.to(DEV)), fa_quantize_e4m3(k.to(DEV)),
+                                     fa_quantize_e4m3(v.to(DEV), per_head=True, transpose=True))
+    o, lse = fa_fwd_e4m3(q8, qd, k8, kd, vt8, vd, causal=causal, q_pos_offset=off, window=window)
+    assert fa_sync_status() == 0
+    qx = e4m3.dequantize_blocks(q8.cpu().numpy(), qd.cpu().numpy())
+    kx = e4m3.dequantize_blocks(k8.cpu().numpy(), kd.cpu().numpy())
+    vx = e4m3.dequantize_blocks(vt8.cpu().numpy()[..., :skv].transpose(0, 3, 1, 2), vd.cpu().numpy(), per_head=True)
+    scale = 1.0 / math.sqrt(d)
+    rows = oracle.all_rows(b, hq, sq)
+    o_ref, l_ref = oracle.attention(qx, kx, vx, causal=causal, q_pos_offset=off, scale=scale, rows=rows,
+                                    window=window if window else (-1, -1))
+    og = o.to(torch.float64).cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+    lg = lse.to(torch.float64).cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    masked = np.isneginf(l_ref)
+    assert np.all(np.isneginf(lg[masked])) and np.all(og[masked] == 0.0), case
+    vis = ~masked
+    tol = e4m3_rounding_bound(qx, kx, vx, causal, off, window, o_ref, l_ref, rows, scale)
+    assert np.all(np.abs(og - o_ref)[vis] <= tol[vis]), case
+    if vis.any():
+        assert np.abs(lg[vis] - l_ref[vis]).max() <= 1e-3, case
