@@ -9,8 +9,10 @@
 // is read once per CTA.  Roles are specialised by warp:
 //   * softmax warpgroups (one per Q tile, one TMEM lane = one query row per
 //     thread): read S from TMEM, mask (diagonal / tail blocks only), update the
-//     running max m and sum l, write P (bf16/fp16) back into the S columns,
-//     rescale the O accumulator, and finally normalise O and write O and LSE;
+//     running max m and sum l, write P (bf16/fp16, or e4m3) back into TMEM (over
+//     the S columns, or for d = 256 into columns of its own), rescale the O
+//     accumulator, and finally normalise O and write O (through shared-memory
+//     slices and TMA stores for d <= 128) and LSE;
 //   * a TMA producer warp: Q tiles once, then K_j, V_j in consumption order;
 //   * an MMA warp: S_t = Q_t K_j^T (both operands in shared memory) and
 //     O_t += P_t V_j (P from TMEM, V from shared memory) with tcgen05, fp32
