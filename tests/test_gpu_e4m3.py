@@ -174,3 +174,39 @@ def test_e4m3_forward_random(i):
     assert np.all(np.abs(og - o_ref)[vis] <= tol[vis]), case
     if vis.any():
         assert np.abs(lg[vis] - l_ref[vis]).max() <= 1e-3, case
+
+
+@pytest.mark.parametrize("name", ["causal_prefill", "ragged_d64", "ragged_d256"])
+def test_e4m3_full_size_on_the_benchmark_inputs(name):
+    """The 8-bit forward at the benchmark's full sizes, on its own inputs quantised
+    the way its e4m3 lines quantise them and in the same launch: one whole head of
+    the last batch and a random sample of rows (with the edge rows) against the
+    per-element bound."""
+    from tiled_exact_attention_gb300 import quantize_qkv_e4m3
+    from tiled_exact_attention_gb300.inputs import WORKLOADS, make_qkv
+    from parity_util import sample_rows
+
+    w = WORKLOADS[name]
+    qc, kc, vc = make_qkv(w)
+    (q8, qd), (k8, kd), (vt8, vd) = quantize_qkv_e4m3(qc.to(DEV), kc.to(DEV), vc.to(DEV))
+    off = w.offset if w.causal else None
+    o, lse = fa_fwd_e4m3(q8, qd, k8, kd, vt8, vd, causal=w.causal, q_pos_offset=off)
+    assert fa_sync_status() == 0
+    qx = e4m3.dequantize_blocks(q8.cpu().numpy(), qd.cpu().numpy())
+    kx = e4m3.dequantize_blocks(k8.cpu().numpy(), kd.cpu().numpy())
+    vx = e4m3.dequantize_blocks(vt8.cpu().numpy()[..., :w.skv].transpose(0, 3, 1, 2), vd.cpu().numpy(),
+                                per_head=True)
+    rows = {tuple(r) for r in sample_rows(w.b, w.hq, w.sq, n_random=512, seed=w.index)}
+    rows.update((w.b - 1, w.hq - 1, i) for i in range(w.sq))
+    rows = np.array(sorted(rows), dtype=np.int64)
+    scale = 1.0 / math.sqrt(w.d)
+    o_ref, l_ref = oracle.attention(qx, kx, vx, causal=w.causal, q_pos_offset=off, scale=scale, rows=rows)
+    og = o.to(torch.float64).cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+    lg = lse.to(torch.float64).cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    masked = np.isneginf(l_ref)
+    assert np.all(np.isneginf(lg[masked])) and np.all(og[masked] == 0.0)
+    vis = ~masked
+    tol = e4m3_rounding_bound(qx, kx, vx, w.causal, off, None, o_ref, l_ref, rows, scale)
+    err = np.abs(og - o_ref)
+    assert np.all(err[vis] <= tol[vis]), f"{name}: O off by {np.max(err[vis] - tol[vis]):.3e} beyond the bound"
+    assert np.abs(lg[vis] - l_ref[vis]).max() <= 1e-3, name
