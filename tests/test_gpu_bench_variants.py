@@ -87,3 +87,51 @@ def test_heads_as_rows_decode_full_size():
     o_ref, l_ref = oracle.attention(f64(qc), f64(kc), f64(vc), causal=False, scale=1.0 / math.sqrt(d), rows=rows)
     og, lg = gather(o, lse, rows)
     assert_parity(og, lg, o_ref, l_ref, qc.dtype, "heads-as-rows decode")
+
+
+@pytest.mark.parametrize("shape", [(1, 32, 8, 128), (8, 32, 8, 64)], ids=["decode_b1", "decode_d64"])
+def test_small_and_d64_decode_full_size(shape):
+    """The decode_b1 and decode_d64 lines: KV = 32768, query at the last position; every row."""
+    b, hq, hkv, d = shape
+    skv = 32768
+    qc, kc, vc = make_custom(b, 1, skv, hq, hkv, d, "bf16", seed=BASE_SEED + 80)
+    o, lse = fa_fwd_splitkv(qc.to(DEV), kc.to(DEV), vc.to(DEV), causal=True, q_pos_offset=skv - 1)
+    assert fa_sync_status() == 0
+    rows = oracle.all_rows(b, hq, 1)
+    o_ref, l_ref = oracle.attention(f64(qc), f64(kc), f64(vc), causal=True, q_pos_offset=skv - 1,
+                                    scale=1.0 / math.sqrt(d), rows=rows)
+    og, lg = gather(o, lse, rows)
+    assert_parity(og, lg, o_ref, l_ref, qc.dtype, f"decode {shape}")
+
+
+def test_paged_decode_full_size():
+    """The decode_paged line: B=8, Hq=32, Hkv=8, d=128, 256-key pages in a shuffled
+    order, lengths 16384-49152; every row, each sequence's pages gathered back for the oracle."""
+    from tiled_exact_attention_gb300 import fa_fwd_kvcache
+
+    b, hq, hkv, d, ps = 8, 32, 8, 128, 256
+    rng = np.random.default_rng(BASE_SEED + 50)
+    lens = rng.integers(16384, 49153, size=b).astype(np.int32)
+    pages_per = [int((n + ps - 1) // ps) for n in lens]
+    num_pages = sum(pages_per)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.zeros((b, max(pages_per)), dtype=np.int32)
+    nxt = 0
+    for i, npg in enumerate(pages_per):
+        table[i, :npg] = perm[nxt:nxt + npg]
+        nxt += npg
+    qc = normal((b, hq, d), BASE_SEED + 50, 0)
+    kc = normal((num_pages, ps, hkv, d), BASE_SEED + 50, 1)
+    vc = normal((num_pages, ps, hkv, d), BASE_SEED + 50, 2)
+    o, lse = fa_fwd_kvcache(qc.to(DEV), kc.to(DEV), vc.to(DEV), block_table=torch.from_numpy(table).to(DEV),
+                            seqlens_k=torch.from_numpy(lens).to(DEV), max_seqlen_k=int(lens.max()))
+    assert fa_sync_status() == 0
+    for i in range(b):
+        n, pages = int(lens[i]), table[i, :pages_per[i]]
+        ks = kc[torch.from_numpy(pages).long()].reshape(-1, hkv, d)[:n][None]
+        vs = vc[torch.from_numpy(pages).long()].reshape(-1, hkv, d)[:n][None]
+        rows = oracle.all_rows(1, hq, 1)
+        o_ref, l_ref = oracle.attention(f64(qc[i][None, None]), f64(ks), f64(vs), scale=1.0 / math.sqrt(d), rows=rows)
+        og = o[i].to(torch.float64).cpu().numpy()
+        lg = lse[i].to(torch.float64).cpu().numpy()
+        assert_parity(og, lg, o_ref, l_ref, qc.dtype, f"paged sequence {i} (length {n})")
