@@ -537,7 +537,7 @@ def bench_backward(dev, flush, steps=30, warmup=3):
     usual 2.5x-forward accounting (five products of 2*d flops per visible pair)."""
     import torch
 
-    from tiled_exact_attention_gb300 import fa_bwd, fa_fwd, fa_sync_status
+    from tiled_exact_attention_gb300 import fa_bwd, fa_bwd_workspace_size, fa_fwd, fa_sync_status
     from tiled_exact_attention_gb300.inputs import BASE_SEED, WORKLOADS, make_qkv, normal
 
     w = WORKLOADS["causal_prefill"]
@@ -545,7 +545,8 @@ def bench_backward(dev, flush, steps=30, warmup=3):
     do = normal(tuple(q.shape), BASE_SEED + w.index, 7, 1.0, q.dtype).to(dev)
     o, lse = fa_fwd(q, k, v, causal=True, q_pos_offset=w.offset)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+    ws = torch.empty(fa_bwd_workspace_size(q, k, v, causal=True, q_pos_offset=w.offset), dtype=torch.uint8,
+                     device=dev)
 
     def step():
         fa_bwd(q, k, v, o, lse, do, causal=True, q_pos_offset=w.offset, dq=dq, dk=dk, dv=dv, workspace=ws)

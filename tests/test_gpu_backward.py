@@ -133,8 +133,11 @@ def test_backward_benchmark_workload():
     q, k, v = (t.to(DEV) for t in make_qkv(w))
     do = normal(tuple(q.shape), BASE_SEED + w.index, 7, 1.0, q.dtype).to(DEV)
     o, lse = fa_fwd(q, k, v, causal=True, q_pos_offset=w.offset)
+    from tiled_exact_attention_gb300 import fa_bwd_workspace_size
+
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(64 << 20, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(fa_bwd_workspace_size(q, k, v, causal=True, q_pos_offset=w.offset), dtype=torch.uint8,
+                     device=DEV)
     fa_bwd(q, k, v, o, lse, do, causal=True, q_pos_offset=w.offset, dq=dq, dk=dk, dv=dv, workspace=ws)
     assert fa_sync_status() == 0
     rq, rk, rv = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), causal=True, q_pos_offset=w.offset,

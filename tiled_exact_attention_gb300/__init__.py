@@ -5,6 +5,7 @@ marshals torch tensors into the C ABI of include/fa.h.
 """
 from .api import (  # noqa: F401
     fa_bwd,
+    fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_kvcache,
     fa_fwd_splitkv,

@@ -311,6 +311,16 @@ def make_bwd_args(q, k, v, o, lse, dout, dq, dk, dv, *, causal: bool, scale: flo
     return a
 
 
+def fa_bwd_workspace_size(q, k, v, *, causal: bool = False, scale: float | None = None,
+                          q_pos_offset: int | None = None, window=None, softcap: float = 0.0) -> int:
+    """Device workspace bytes fa_bwd needs for these shapes (D and L * log2(e) per padded row)."""
+    b, sq, hq, _ = q.shape
+    lse = torch.empty((b, hq, sq), dtype=torch.float32, device=q.device)
+    a = make_bwd_args(q, k, v, q, lse, q, q, k, v, causal=causal, scale=scale, q_pos_offset=q_pos_offset,
+                      window=window, softcap=softcap)
+    return int(_lib.load().fa_bwd_workspace_size(ctypes.byref(a)))
+
+
 def fa_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: float | None = None,
            q_pos_offset: int | None = None, window=None, dq=None, dk=None, dv=None, workspace=None, stream=None,
            softcap: float = 0.0):
