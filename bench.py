@@ -19,9 +19,8 @@ rank's time.
 Every roofline divides by the measured burst bf16 GEMM peak (each launch lasts
 well under a millisecond, between L2 flushes); the sustained peak is reported
 beside it.  `--only NAME[,NAME...]` times just the named lines (prefill, decode,
-gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, e4m3_d256, paged, decode_e4m3, variants, e2e,
-link)
-and prints them as one JSON object: the form the ncu captures use.
+gqa_long, ragged_d64, ragged_d256, backward, e4m3, e4m3_d64, e4m3_d256, paged, decode_e4m3, variants,
+decode_b1, decode_d64, e2e, link) and prints them as one JSON object: the form the ncu captures use.
 """
 from __future__ import annotations
 
@@ -206,7 +205,7 @@ def _setup(args):
 
 
 SECONDARY = ("gqa_long", "ragged_d64", "ragged_d256", "paged", "decode_e4m3", "backward", "e4m3", "e4m3_d64", "e4m3_d256",
-             "variants", "e2e", "link")
+             "variants", "decode_b1", "decode_d64", "e2e", "link")
 
 
 def run_only(args):
@@ -235,6 +234,8 @@ def run_only(args):
             out[nm] = bench_e4m3(dev, flush, steps=steps, warmup=args.warmup, workload="ragged_" + nm[5:])
         elif nm == "variants":
             out[nm] = bench_variants(dev, flush, steps=steps)
+        elif nm in SMALL_DECODES:
+            out[nm] = bench_small_decode(dev, flush, nm, steps=steps)
         elif nm in ("e2e", "link"):
             from tiled_exact_attention_gb300 import fa_fwd
             from tiled_exact_attention_gb300.inputs import make_qkv
@@ -753,29 +754,48 @@ def bench_variants(dev, flush, steps=20):
                                    "kernels": "fa_prefill_kernel (heads as rows) + fa_combine_kernel"},
                         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                                      "frac": round(gbs / hbm, 4), "traffic": None}}
-    # split-KV decode at a small batch (B = 1, the decode workload otherwise) and at d = 64 (B = 8, Hq = 32,
-    # Hkv = 8, KV = 32768): KV GB/s against the measured copy peak
-    for key, (b, hq, hkv, d) in (("decode_b1", (1, 32, 8, 128)), ("decode_d64", (8, 32, 8, 64))):
-        skv = 32768
-        qd, kd, vd = (t.to(dev) for t in make_custom(b, 1, skv, hq, hkv, d, "bf16", seed=BASE_SEED + 80))
-        od = torch.empty_like(qd)
-        ld = torch.empty((b, hq, 1), dtype=torch.float32, device=dev)
-        work = torch.empty(fa_splitkv_workspace_size(qd, kd, vd, 0, causal=True, q_pos_offset=skv - 1),
-                           dtype=torch.uint8, device=dev)
-        used = fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od, lse=ld,
-                              return_splits=True)[2]
-        ms = _timed(lambda: fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od,
-                                           lse=ld), flush, steps)
-        nbytes = 2 * b * skv * hkv * d * 2 + 2 * b * hq * d * 2 + b * hq * 4
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        out[key] = {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
-                    "config": {"b": b, "skv": skv, "hq": hq, "hkv": hkv, "d": d, "num_splits": used},
-                    "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                                 "frac": round(gbs / hbm, 4), "traffic": None}}
-        del qd, kd, vd, work
+    del qd, kd, vd, work
+    for key in SMALL_DECODES:
+        out[key] = bench_small_decode(dev, flush, key, steps)
     if fa_sync_status() != 0:
         raise RuntimeError("device status set by a forward-pass variant")
     return out
+
+
+SMALL_DECODES = {"decode_b1": (1, 32, 8, 128), "decode_d64": (8, 32, 8, 64)}  # b, hq, hkv, d
+
+
+def bench_small_decode(dev, flush, key, steps=30):
+    """Split-KV decode at a small batch (decode_b1: B = 1, the decode workload otherwise) or at d = 64
+    (decode_d64: B = 8, Hq = 32, Hkv = 8): KV = 32768, the query at the last position; KV GB/s against the
+    measured copy peak."""
+    import torch
+
+    from tiled_exact_attention_gb300 import fa_fwd_splitkv, fa_sync_status
+    from tiled_exact_attention_gb300.api import fa_splitkv_workspace_size
+    from tiled_exact_attention_gb300.inputs import BASE_SEED, make_custom
+
+    b, hq, hkv, d = SMALL_DECODES[key]
+    skv = 32768
+    qd, kd, vd = (t.to(dev) for t in make_custom(b, 1, skv, hq, hkv, d, "bf16", seed=BASE_SEED + 80))
+    od = torch.empty_like(qd)
+    ld = torch.empty((b, hq, 1), dtype=torch.float32, device=dev)
+    work = torch.empty(fa_splitkv_workspace_size(qd, kd, vd, 0, causal=True, q_pos_offset=skv - 1),
+                       dtype=torch.uint8, device=dev)
+    used = fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od, lse=ld,
+                          return_splits=True)[2]
+    ms = _timed(lambda: fa_fwd_splitkv(qd, kd, vd, causal=True, q_pos_offset=skv - 1, workspace=work, out=od,
+                                       lse=ld), flush, steps)
+    if fa_sync_status() != 0:
+        raise RuntimeError(f"device status set by {key}")
+    nbytes = 2 * b * skv * hkv * d * 2 + 2 * b * hq * d * 2 + b * hq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = float(_peaks()[0]["hbm_gbs"])
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "config": {"b": b, "skv": skv, "hq": hq, "hkv": hkv, "d": d, "num_splits": used},
+            "bytes_per_launch": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": _profiled_traffic("fa_decode_kernel_" + key[7:])}}
 
 
 def bench_e2e(qc, kc, vc, wp, fa_fwd, flush, stream, steps, dist=None):
