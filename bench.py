@@ -80,16 +80,24 @@ def _dist():
     return ws, rank, local
 
 
-def _kernel_source_hash() -> str:
+# The sources each profiled kernel family is compiled from: a capture stays valid
+# while these files are unchanged.
+KERNEL_SOURCES = {
+    "fa_prefill_kernel": ("fa_prefill.cu", "ptx.cuh", "fa_internal.h", "tc_common.cuh"),
+    "fa_decode_kernel": ("fa_decode.cu", "ptx.cuh", "fa_internal.h"),
+    "fa_bwd_": ("fa_backward.cu", "ptx.cuh", "fa_internal.h", "tc_common.cuh"),
+}
+
+
+def _kernel_source_hash(kernel: str) -> str | None:
+    family = next((k for k in KERNEL_SOURCES if kernel.startswith(k)), None)
+    if family is None:
+        return None
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "tiled_exact_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
-
-
-KERNEL_SOURCES = ("fa_prefill.cu", "fa_decode.cu", "fa_backward.cu", "fa_fp8.cu", "ptx.cuh", "fa_internal.h",
-                  "tc_common.cuh")
 
 
 def _profiled_traffic(kernel: str):
@@ -98,7 +106,9 @@ def _profiled_traffic(kernel: str):
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
-    want = _kernel_source_hash()
+    want = _kernel_source_hash(kernel)
+    if want is None:
+        return None
     with open(p) as f:
         for line in f:
             parts = line.strip().strip("|").split("|")
@@ -574,7 +584,7 @@ def bench_backward(dev, flush, steps=30, warmup=3):
             "flops_per_launch": flops, "flops_executed_per_launch": 3.5 * 4.0 * w.d * pairs,
             "accounting": "2.5x the forward flops (dV, dP, dQ, dK and the recomputed S); the kernels execute 3.5x "
                           "(S and dP are recomputed by both the dQ and the dK/dV kernel)",
-            "kernels": "fa_bwd_pre_kernel + fa_bwd_dq_kernel + fa_bwd_dkdv_kernel", "steps": steps}
+            "kernels": "fa_bwd_dq_kernel (also forms D and L per row) + fa_bwd_dkdv_kernel", "steps": steps}
 
 
 def bench_e4m3(dev, flush, steps=30, warmup=3, workload="causal_prefill"):

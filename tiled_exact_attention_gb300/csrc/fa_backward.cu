@@ -5,11 +5,11 @@
 // recovers P = exp(S - L), and forms
 //   D = rowsum(dO * O), dP = dO V^T, dS = P (dP - D),
 //   dV = P^T dO, dQ = dS K * scale, dK = dS^T Q * scale,
-// with P and dS zero where the mask hides a key.  Three kernels:
-//   * fa_bwd_pre_kernel: D and L * log2(e) per row (HBM-bound, one warp per row);
+// with P and dS zero where the mask hides a key.  Two kernels:
 //   * fa_bwd_dq_kernel: a CTA owns 128 query rows and streams the key blocks
 //     they see (S = Q K^T, dP = dO V^T, dQ += dS K on tcgen05, one TMEM lane per
-//     row for the elementwise work);
+//     row for the elementwise work); its elementwise threads first form D and
+//     L * log2(e) of their rows, which it also writes for the second kernel;
 //   * fa_bwd_dkdv_kernel: a CTA owns 128 keys of one key/value head and streams
 //     the query tiles that see them, over every query head of its group (S^T =
 //     K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q, one TMEM lane per key),
@@ -84,82 +84,33 @@ struct BwdCfg {
   static_assert(ACC_COL + 2 * D <= TMEM_COLS, "dK and dV accumulators must fit in TMEM");
 };
 
-// ------------------------------------------------------------------ preprocess
+// ------------------------------------------------------------------ row terms
 
-// D = sum_t dO_t O_t in fp32 from the stored (rounded) O, and L2 = LSE * log2(e),
-// per (batch, head, padded row); padding rows and rows that see no key get
-// L2 = +inf, so that every probability recovered from it is 0.  D / 8 lanes per
-// row with 16-byte loads, several rows per warp in flight (the pass is bound by
-// HBM, not by its arithmetic).
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
-  constexpr int LPR = D / 8;        // lanes per row
-  constexpr int RPW = 32 / LPR;     // rows per warp per step
-  constexpr int UNROLL = 2;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / LPR, li = lane % LPR;
-  const int64_t nrows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * 8 * RPW * UNROLL;
-  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * RPW * UNROLL; base < nrows; base += step) {
-    float dsum[UNROLL], l2[UNROLL];
-    uint4 ou[UNROLL], du[UNROLL];
-    int64_t rowid[UNROLL];
+// acc + sum of the 8 products of two rows' 16-bit values (widened exactly to fp32).
+template <bool BF16>
+__device__ __forceinline__ float dot8(const uint4 a, const uint4 b, float acc) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int64_t row = base + u * RPW + sub;
-      rowid[u] = row;
-      ou[u] = du[u] = make_uint4(0u, 0u, 0u, 0u);
-      l2[u] = INFINITY;
-      if (row < nrows) {
-        const int i = static_cast<int>(row % p.sq_pad);
-        const int64_t bh = row / p.sq_pad;
-        const int h = static_cast<int>(bh % p.hq), bi = static_cast<int>(bh / p.hq);
-        if (i < p.sq) {
-          ou[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + bi * p.o_st[0] +
-                                                  static_cast<int64_t>(i) * p.o_st[1] + h * p.o_st[2] + li * 8);
-          du[u] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + bi * p.do_st[0] +
-                                                  static_cast<int64_t>(i) * p.do_st[1] + h * p.do_st[2] + li * 8);
-          const float lse = p.lse[bh * p.sq + i];
-          l2[u] = lse > -INFINITY ? lse * kLog2e : INFINITY;
-        }
-      }
+  for (int e = 0; e < 4; ++e) {
+    float a0, a1, b0, b1;
+    if constexpr (BF16) {
+      a0 = __uint_as_float(aw[e] << 16);
+      a1 = __uint_as_float(aw[e] & 0xffff0000u);
+      b0 = __uint_as_float(bw[e] << 16);
+      b1 = __uint_as_float(bw[e] & 0xffff0000u);
+    } else {
+      const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&aw[e]));
+      const float2 bf = __half22float2(*reinterpret_cast<const __half2*>(&bw[e]));
+      a0 = af.x;
+      a1 = af.y;
+      b0 = bf.x;
+      b1 = bf.y;
     }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const uint32_t ow[4] = {ou[u].x, ou[u].y, ou[u].z, ou[u].w};
-      const uint32_t dw[4] = {du[u].x, du[u].y, du[u].z, du[u].w};
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float o0, o1, d0, d1;
-        if constexpr (BF16) {
-          o0 = __uint_as_float(ow[e] << 16);
-          o1 = __uint_as_float(ow[e] & 0xffff0000u);
-          d0 = __uint_as_float(dw[e] << 16);
-          d1 = __uint_as_float(dw[e] & 0xffff0000u);
-        } else {
-          const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[e]));
-          const float2 df = __half22float2(*reinterpret_cast<const __half2*>(&dw[e]));
-          o0 = of.x;
-          o1 = of.y;
-          d0 = df.x;
-          d1 = df.y;
-        }
-        acc = fmaf(o0, d0, acc);
-        acc = fmaf(o1, d1, acc);
-      }
-#pragma unroll
-      for (int x = LPR / 2; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
-      dsum[u] = acc;
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      if (li == 0 && rowid[u] < nrows) {
-        p.dpre[rowid[u]] = dsum[u];
-        p.l2pre[rowid[u]] = l2[u];
-      }
-    }
+    acc = fmaf(a0, b0, acc);
+    acc = fmaf(a1, b1, acc);
   }
+  return acc;
 }
 
 // Store NC fp32 values (scaled by `mul`) from TMEM columns [tcol, tcol + NC) of
@@ -362,14 +313,54 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dq_kernel(const 
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tP = tbase + lane_off + C::DP_COL;
     const int64_t prow = (static_cast<int64_t>(bi) * p.hq + h) * p.sq_pad + row;  // row < sq_pad
-    const float l2 = p.l2pre[prow];
-    const float dd = p.dpre[prow];
+    // D = rowsum(dO * O) over the stored (rounded) O and L2 = LSE * log2(e) of this
+    // row: O's row is loaded from global memory at once, dO's is read from the
+    // tile the producer stages (from global memory too when no key block is
+    // visited); both warpgroups form them and the first writes them for the
+    // dK / dV kernel (which runs after this one).  Padding rows and rows that see
+    // no key get L2 = +inf (every probability recovered from it is 0) and D = 0.
+    bool ok = true;
+    float l2 = INFINITY, dd = 0.f;
+    {
+      constexpr int NC = D / 8;
+      const bool live = row < p.sq;
+      uint4 ov[NC];
+      float lse = -INFINITY;
+      if (live) {
+        lse = p.lse[(static_cast<int64_t>(bi) * p.hq + h) * p.sq + row];
+        const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + bi * p.o_st[0] +
+                                                         static_cast<int64_t>(row) * p.o_st[1] + h * p.o_st[2]);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) ov[c] = o4[c];
+      }
+      if (N > 0) {
+        ok = warp_wait(q_full, 0, p.status, kSiteBwdQFull);
+        if (ok && live) {
+          const uint8_t* dtile = smem + C::TILE_BYTES;  // 64-column chunks of 128-byte rows, 128-byte swizzle
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            dd = dot8<BF16>(ov[c],
+                            *reinterpret_cast<const uint4*>(dtile + (c / 8) * (BM * 128) + r * 128 +
+                                                            (((c % 8) ^ (r & 7)) << 4)),
+                            dd);
+        }
+      } else if (live) {
+        const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + bi * p.do_st[0] +
+                                                         static_cast<int64_t>(row) * p.do_st[1] + h * p.do_st[2]);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) dd = dot8<BF16>(ov[c], g4[c], dd);
+      }
+      if (live) l2 = lse > -INFINITY ? lse * kLog2e : INFINITY;
+    }
+    if (eg == 0) {
+      p.dpre[prow] = dd;
+      p.l2pre[prow] = l2;
+    }
     const float sl2 = p.scale_log2;
     // keys lo_row <= j < lim_row are visible to this row
     const int lim_row = p.causal ? min(p.skv, max(row + p.off + 1, 0)) : p.skv;
     const int lo_row = p.local ? row + p.left_off : 0;
-    bool ok = true;
-    for (int it = 0; it < N; ++it) {
+    for (int it = 0; ok && it < N; ++it) {
       const int n = n_hi - 1 - it;
       const uint32_t tSb = tbase + lane_off + ((it & 1) ? C::S2_COL : C::S_COL);  // this block's S buffer
       // ---- P = 2^(S scale log2 e - L2) as soon as S is in TMEM ----
@@ -802,14 +793,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) fa_bwd_dkdv_kernel(cons
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  {
-    const int64_t rows = static_cast<int64_t>(p.b) * p.hq * p.sq_pad;
-    const int64_t blocks = (rows + 8 * 2 * (256 / D) - 1) / (8 * 2 * (256 / D));  // rows per CTA step
-    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
-    if (grid > 0) fa_bwd_pre_kernel<D, BF16><<<grid, 256, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   {
     auto kern = p.sc_b > 0.f ? fa_bwd_dq_kernel<D, BF16, true> : fa_bwd_dq_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DQ_SMEM);
